@@ -1,0 +1,53 @@
+/*
+ * matrixopt_debug.h -- introspection entry points for tests.  They expose
+ * where the Newton-Schulz intermediates live inside a workspace so that a
+ * test can check each phase (the Gram matrix X X^T, the polynomial
+ * b*A + c*A^2, the applied X) separately.  The pages have no counterpart;
+ * these calls compute nothing.
+ */
+#ifndef MATRIXOPT_DEBUG_H
+#define MATRIXOPT_DEBUG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Placement of matrix `index`'s Newton-Schulz buffers in the workspace that
+ * ns_orthogonalize / muon_step_batched use for these shapes (offsets are in
+ * bytes from the workspace base).  Orientation: m = min(rows, cols),
+ * n = max(rows, cols), transposed = rows > cols.
+ *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong (ldx),
+ *              x_master = fp32 m x n (ldx), gram = bf16 m x m (lda),
+ *              poly = bf16 m x m (lda).
+ *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong (x_master = 0),
+ *              gram, poly = fp32 m x m.
+ * After a call with steps = 1 the gram buffer holds X0 X0^T and the poly
+ * buffer b*A + c*A*A of that step. */
+typedef struct {
+    int64_t m, n, ldx, lda;
+    int32_t transposed, precision;
+    int64_t x_op[2], x_master, gram, poly;
+} mo_ns_view;
+
+int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precision,
+                     int index, mo_ns_view* view);
+
+/* Number of SMs the grouped kernels size their grids for on the current
+ * device (0 if no device). */
+int mo_debug_sm_count(void);
+
+/* Chooses between the two readings of the shared-memory descriptor strides
+ * for the MN-major operand of the apply phase (64-element MN atoms 8 KB
+ * apart, 8-row K groups 1 KB apart): (lbo, sbo) = (8192, 1024), the default,
+ * or (1024, 8192).  Other values give MO_ERR_INVALID_ARG.  Process-wide;
+ * affects launches issued after the call. */
+int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MATRIXOPT_DEBUG_H */

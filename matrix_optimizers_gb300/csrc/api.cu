@@ -1,0 +1,717 @@
+// Host side of the C ABI: argument validation, workspace layout, tensor-map
+// encoding, tile scheduling across SMs, launch sequencing, the owner planner.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <queue>
+#include <vector>
+
+#include "../../include/matrixopt.h"
+#include "../../include/matrixopt_debug.h"
+#include "internal.h"
+
+namespace mo {
+
+namespace {
+
+constexpr int64_t kMaxMinDim = 32768;        // m = min(rows, cols): the m x m buffers
+constexpr int64_t kMaxDim = 1 << 20;
+constexpr size_t kWsAlign = 256;
+constexpr size_t kBufAlign = 1024;
+constexpr size_t kHeaderBytes = 256;         // int error word + reserved
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t elem_size(int dt) { return dt == MO_F32 ? 4 : 2; }
+inline bool valid_dtype(int dt) { return dt == MO_F32 || dt == MO_BF16; }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? MO_OK : MO_ERR_CUDA; }
+
+// ------------------------------------------------------------ device info
+int g_sm_count_cache[64];
+std::once_flag g_sm_once[64];
+
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::call_once(g_sm_once[dev], [dev] {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) c = 1;
+        g_sm_count_cache[dev] = c;
+    });
+    return g_sm_count_cache[dev];
+}
+
+namespace {
+
+// ------------------------------------------------------- tensor-map encode
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+// bf16 rows x cols (leading dim ld elements), box 64 x 64, 128-byte swizzle.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    cuuint32_t box[2] = {64, 64};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Descriptor strides of the MN-major B operand (64-element MN atoms of 8 KB,
+// 8-row K groups of 1 KB).  Exposed to tests through the debug header.
+std::atomic<uint32_t> g_mn_lbo{8192};
+std::atomic<uint32_t> g_mn_sbo{1024};
+
+// ------------------------------------------------------------- the request
+struct Job {
+    int64_t rows, cols, ld;
+    int src_dtype, g_dtype, w_dtype, out_dtype;
+    int has_momentum;
+    void* src;
+    const void* grad;
+    void* W;
+    void* out;
+};
+
+struct Shape {
+    int64_t m, n, ldx, lda;
+    int transposed;
+};
+
+Shape oriented(int64_t rows, int64_t cols) {
+    Shape s;
+    s.transposed = rows > cols;
+    s.m = s.transposed ? cols : rows;
+    s.n = s.transposed ? rows : cols;
+    s.ldx = static_cast<int64_t>(align_up(static_cast<size_t>(s.n), 64));
+    s.lda = static_cast<int64_t>(align_up(static_cast<size_t>(s.m), 64));
+    return s;
+}
+
+struct MatBufs {
+    size_t x_op[2], x_master, gram, poly;
+};
+
+// Counts of tiles per phase for one matrix.
+int64_t sym_tiles(int64_t m) {
+    int64_t cnt = 0;
+    const int64_t tr = ceil_div(m, kTcBM), tc = ceil_div(m, kTcBN);
+    for (int64_t I = 0; I < tr; ++I)
+        for (int64_t J = 0; J < tc; ++J)
+            if (std::min(J * kTcBN + kTcBN - 1, m - 1) >= I * kTcBM) ++cnt;
+    return cnt;
+}
+
+struct Layout {
+    int precision;
+    size_t mats, tmaps, tiles[3], ranges[3], partials, scales, bufs_begin, total;
+    size_t ctl_bytes;              // [0, ctl_bytes) is uploaded every call
+    int64_t ntiles[3];
+    int64_t mom_tiles;
+    std::vector<MatBufs> buf;
+    std::vector<Shape> shape;
+};
+
+Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int precision) {
+    Layout L;
+    L.precision = precision;
+    const size_t n = dims.size();
+    L.shape.resize(n);
+    L.buf.resize(n);
+    L.ntiles[0] = L.ntiles[1] = L.ntiles[2] = 0;
+    L.mom_tiles = 0;
+    for (size_t i = 0; i < n; ++i) {
+        const Shape s = oriented(dims[i].first, dims[i].second);
+        L.shape[i] = s;
+        L.mom_tiles += ceil_div(dims[i].first, kMomTile) * ceil_div(dims[i].second, kMomTile);
+        if (precision == MO_NS_BF16) {
+            const int64_t st = sym_tiles(s.m);
+            L.ntiles[0] += st;
+            L.ntiles[1] += st;
+            L.ntiles[2] += ceil_div(s.m, kTcBM) * ceil_div(s.n, kTcBN);
+        } else {
+            const int64_t t = ceil_div(s.m, kFpBM);
+            L.ntiles[0] += t * t;
+            L.ntiles[1] += t * t;
+            L.ntiles[2] += t * ceil_div(s.n, kFpBN);
+        }
+    }
+    size_t off = kHeaderBytes;
+    L.mats = off;
+    off = align_up(off + n * sizeof(MatDesc), 128);
+    L.tmaps = off;
+    if (precision == MO_NS_BF16) off = align_up(off + n * 4 * sizeof(CUtensorMap), 128);
+    for (int ph = 0; ph < 3; ++ph) {
+        L.tiles[ph] = off;
+        off = align_up(off + static_cast<size_t>(L.ntiles[ph]) * sizeof(TileDesc), 128);
+        L.ranges[ph] = off;
+        off = align_up(off + static_cast<size_t>(L.ntiles[ph]) * sizeof(int2), 128);
+    }
+    L.ctl_bytes = off;
+    L.partials = off;
+    off = align_up(off + static_cast<size_t>(L.mom_tiles) * sizeof(float), 128);
+    L.scales = off;
+    off = align_up(off + n * 2 * sizeof(float), kBufAlign);
+    L.bufs_begin = off;
+    const size_t xe = precision == MO_NS_BF16 ? 2 : 4;
+    for (size_t i = 0; i < n; ++i) {
+        const Shape& s = L.shape[i];
+        const size_t xbytes = static_cast<size_t>(s.m) * s.ldx * xe;
+        const size_t abytes = static_cast<size_t>(s.m) * s.lda * xe;
+        MatBufs& b = L.buf[i];
+        b.x_op[0] = off; off = align_up(off + xbytes, kBufAlign);
+        b.x_op[1] = off; off = align_up(off + xbytes, kBufAlign);
+        if (precision == MO_NS_BF16) {
+            b.x_master = off;
+            off = align_up(off + static_cast<size_t>(s.m) * s.ldx * 4, kBufAlign);
+        } else {
+            b.x_master = 0;
+        }
+        b.gram = off; off = align_up(off + abytes, kBufAlign);
+        b.poly = off; off = align_up(off + abytes, kBufAlign);
+    }
+    L.total = off;
+    return L;
+}
+
+// LPT assignment of tiles to CTAs: tiles sorted by cost (descending, then
+// matrix / row / column), each to the least-loaded CTA (ties: lower index).
+void schedule(std::vector<TileDesc>& tiles, int ctas, int epi_cost, std::vector<TileDesc>& out,
+              std::vector<int2>& ranges) {
+    std::stable_sort(tiles.begin(), tiles.end(), [](const TileDesc& a, const TileDesc& b) {
+        return a.nkb > b.nkb;
+    });
+    using Item = std::pair<int64_t, int>;
+    std::priority_queue<Item, std::vector<Item>, std::greater<Item>> heap;
+    for (int c = 0; c < ctas; ++c) heap.push({0, c});
+    std::vector<std::vector<int>> per(ctas);
+    for (size_t t = 0; t < tiles.size(); ++t) {
+        Item it = heap.top();
+        heap.pop();
+        per[it.second].push_back(static_cast<int>(t));
+        it.first += tiles[t].nkb + epi_cost;
+        heap.push(it);
+    }
+    out.clear();
+    ranges.assign(ctas, make_int2(0, 0));
+    for (int c = 0; c < ctas; ++c) {
+        ranges[c].x = static_cast<int>(out.size());
+        ranges[c].y = static_cast<int>(per[c].size());
+        for (int t : per[c]) out.push_back(tiles[t]);
+    }
+}
+
+int validate_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kWsAlign) != 0) return MO_ERR_WORKSPACE;
+    if (ws_bytes < need) return MO_ERR_WORKSPACE;
+    return MO_OK;
+}
+
+int validate_dims(int64_t rows, int64_t cols, int64_t ld) {
+    if (rows < 0 || cols < 0 || ld < 0) return MO_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (ld < cols) return MO_ERR_INVALID_ARG;
+    if (std::min(rows, cols) > kMaxMinDim || std::max(rows, cols) > kMaxDim) return MO_ERR_UNSUPPORTED;
+    return MO_OK;
+}
+
+int validate_buffer(const void* p, int dt, int64_t ld) {
+    if (!valid_dtype(dt)) return MO_ERR_INVALID_ARG;
+    if (p == nullptr) return MO_ERR_INVALID_ARG;
+    if (!aligned16(p) || (static_cast<size_t>(ld) * elem_size(dt)) % 16 != 0) return MO_ERR_ALIGNMENT;
+    return MO_OK;
+}
+
+int validate_tail(const mo_adamw_tail* t) {
+    if (t == nullptr) return MO_OK;
+    if (t->numel < 0) return MO_ERR_INVALID_ARG;
+    if (t->numel == 0) return MO_OK;
+    if (t->step < 1) return MO_ERR_INVALID_ARG;
+    if (!t->W || !t->g || !t->m || !t->v) return MO_ERR_INVALID_ARG;
+    if (!aligned16(t->W) || !aligned16(t->g) || !aligned16(t->m) || !aligned16(t->v)) return MO_ERR_ALIGNMENT;
+    return MO_OK;
+}
+
+struct NsOpts {
+    int precision, steps, apply_update;
+    float mu, a, b, c, alpha, decay;
+};
+
+thread_local std::vector<uint8_t> t_stage;
+
+// Builds the control block for `jobs`, uploads it into `ws` and launches the
+// whole path on `stream`.
+int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    std::vector<std::pair<int64_t, int64_t>> dims;
+    dims.reserve(jobs.size());
+    for (const Job& j : jobs) dims.push_back({j.rows, j.cols});
+    if (jobs.empty()) return MO_OK;
+    const Layout L = make_layout(dims, o.precision);
+    int st = validate_ws(ws, ws_bytes, L.total);
+    if (st != MO_OK) return st;
+    if (o.precision == MO_NS_BF16 && !get_encode()) return MO_ERR_CUDA;
+
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const int nsm = device_sm_count();
+    t_stage.assign(L.ctl_bytes, 0);
+    uint8_t* h = t_stage.data();
+    MatDesc* hm = reinterpret_cast<MatDesc*>(h + L.mats);
+    CUtensorMap* htm = reinterpret_cast<CUtensorMap*>(h + L.tmaps);
+    const CUtensorMap* dtm = reinterpret_cast<const CUtensorMap*>(base + L.tmaps);
+
+    int64_t mom_begin = 0;
+    for (size_t i = 0; i < jobs.size(); ++i) {
+        const Job& j = jobs[i];
+        const Shape& s = L.shape[i];
+        const MatBufs& b = L.buf[i];
+        MatDesc& d = hm[i];
+        d.m = static_cast<int32_t>(s.m);
+        d.n = static_cast<int32_t>(s.n);
+        d.ldx = static_cast<int32_t>(s.ldx);
+        d.lda = static_cast<int32_t>(s.lda);
+        d.ld = j.ld;
+        d.rows = static_cast<int32_t>(j.rows);
+        d.cols = static_cast<int32_t>(j.cols);
+        d.transposed = s.transposed;
+        d.src_dtype = j.src_dtype;
+        d.g_dtype = j.g_dtype;
+        d.w_dtype = j.w_dtype;
+        d.out_dtype = j.out_dtype;
+        d.has_momentum = j.has_momentum;
+        d.src = j.src;
+        d.grad = j.grad;
+        d.W = j.W;
+        d.out = j.out;
+        d.x_op[0] = base + b.x_op[0];
+        d.x_op[1] = base + b.x_op[1];
+        d.x_master = o.precision == MO_NS_BF16 ? reinterpret_cast<float*>(base + b.x_master) : nullptr;
+        d.gram = base + b.gram;
+        d.poly = base + b.poly;
+        d.scales = reinterpret_cast<float*>(base + L.scales) + 2 * i;
+        d.mom_tile_begin = mom_begin;
+        d.mom_tiles_r = static_cast<int32_t>(ceil_div(j.rows, kMomTile));
+        d.mom_tiles_c = static_cast<int32_t>(ceil_div(j.cols, kMomTile));
+        mom_begin += static_cast<int64_t>(d.mom_tiles_r) * d.mom_tiles_c;
+        if (o.precision == MO_NS_BF16) {
+            for (int q = 0; q < 2; ++q) {
+                if (!encode_bf16_map(&htm[4 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
+                d.tm_x[q] = dtm + 4 * i + q;
+            }
+            if (!encode_bf16_map(&htm[4 * i + 2], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&htm[4 * i + 3], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            d.tm_gram = dtm + 4 * i + 2;
+            d.tm_poly = dtm + 4 * i + 3;
+        } else {
+            d.tm_x[0] = d.tm_x[1] = d.tm_gram = d.tm_poly = nullptr;
+        }
+    }
+
+    // tile lists per phase
+    int grids[3] = {0, 0, 0};
+    for (int ph = 0; ph < 3; ++ph) {
+        std::vector<TileDesc> tiles;
+        tiles.reserve(static_cast<size_t>(L.ntiles[ph]));
+        for (size_t i = 0; i < jobs.size(); ++i) {
+            const Shape& s = L.shape[i];
+            if (o.precision == MO_NS_BF16) {
+                const int nkb = static_cast<int>(ceil_div(ph == kGram ? s.n : s.m, kTcBK));
+                const int64_t tr = ceil_div(s.m, kTcBM);
+                const int64_t tc = ceil_div(ph == kApply ? s.n : s.m, kTcBN);
+                for (int64_t I = 0; I < tr; ++I)
+                    for (int64_t J = 0; J < tc; ++J) {
+                        if (ph != kApply && std::min(J * kTcBN + kTcBN - 1, s.m - 1) < I * kTcBM) continue;
+                        tiles.push_back(TileDesc{static_cast<int32_t>(i), static_cast<int32_t>(I),
+                                                 static_cast<int32_t>(J), nkb});
+                    }
+            } else {
+                const int nkb = static_cast<int>(ceil_div(ph == kGram ? s.n : s.m, kFpBK));
+                const int64_t tr = ceil_div(s.m, kFpBM);
+                const int64_t tc = ceil_div(ph == kApply ? s.n : s.m, kFpBN);
+                for (int64_t I = 0; I < tr; ++I)
+                    for (int64_t J = 0; J < tc; ++J)
+                        tiles.push_back(TileDesc{static_cast<int32_t>(i), static_cast<int32_t>(I),
+                                                 static_cast<int32_t>(J), nkb});
+            }
+        }
+        TileDesc* ht = reinterpret_cast<TileDesc*>(h + L.tiles[ph]);
+        if (o.precision == MO_NS_BF16) {
+            const int ctas = static_cast<int>(std::min<int64_t>(nsm, static_cast<int64_t>(tiles.size())));
+            std::vector<TileDesc> sorted;
+            std::vector<int2> ranges;
+            schedule(tiles, ctas, ph == kApply ? 6 : 4, sorted, ranges);
+            std::memcpy(ht, sorted.data(), sorted.size() * sizeof(TileDesc));
+            std::memcpy(h + L.ranges[ph], ranges.data(), ranges.size() * sizeof(int2));
+            grids[ph] = ctas;
+        } else {
+            std::memcpy(ht, tiles.data(), tiles.size() * sizeof(TileDesc));
+            grids[ph] = static_cast<int>(tiles.size());
+        }
+    }
+
+    cudaError_t e = cudaMemcpyAsync(base, h, L.ctl_bytes, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return MO_ERR_CUDA;
+
+    const MatDesc* dmats = reinterpret_cast<const MatDesc*>(base + L.mats);
+    MomLaunch mp;
+    mp.mats = dmats;
+    mp.nmats = static_cast<int32_t>(jobs.size());
+    mp.ntiles = L.mom_tiles;
+    mp.mu = o.mu;
+    mp.fp32_operand = o.precision == MO_NS_FP32;
+    mp.partials = reinterpret_cast<float*>(base + L.partials);
+    const int mom_grid = static_cast<int>(std::min<int64_t>(L.mom_tiles, static_cast<int64_t>(nsm) * 8));
+    if ((e = launch_momentum_norm(mp, mom_grid, stream)) != cudaSuccess) return MO_ERR_CUDA;
+    if ((e = launch_norm_finalize(dmats, mp.nmats, mp.partials, stream)) != cudaSuccess) return MO_ERR_CUDA;
+
+    if (o.steps == 0) {
+        e = launch_ns_k0(mp, o.alpha, o.decay, o.apply_update, mom_grid, stream);
+        return map_cuda(e);
+    }
+    NsLaunch np;
+    np.mats = dmats;
+    np.err = reinterpret_cast<int*>(base);
+    np.steps = o.steps;
+    np.apply_update = o.apply_update;
+    np.a = o.a;
+    np.b = o.b;
+    np.c = o.c;
+    np.alpha = o.alpha;
+    np.decay = o.decay;
+    np.mn_lbo = g_mn_lbo.load();
+    np.mn_sbo = g_mn_sbo.load();
+    for (int t = 0; t < o.steps; ++t) {
+        for (int ph = 0; ph < 3; ++ph) {
+            np.phase = ph;
+            np.step = t;
+            np.tiles = reinterpret_cast<const TileDesc*>(base + L.tiles[ph]);
+            np.cta_range = reinterpret_cast<const int2*>(base + L.ranges[ph]);
+            np.ntiles = static_cast<int32_t>(L.ntiles[ph]);
+            np.idesc = idesc_bf16_f32(kTcBM, kTcBN, ph == kApply ? 1u : 0u);
+            e = o.precision == MO_NS_BF16 ? launch_ns_tc_phase(np, grids[ph], stream)
+                                          : launch_ns_fp32_phase(np, grids[ph], stream);
+            if (e != cudaSuccess) return MO_ERR_CUDA;
+        }
+    }
+    return MO_OK;
+}
+
+int ns_workspace_for(const std::vector<std::pair<int64_t, int64_t>>& dims, int precision, size_t* out) {
+    if (out == nullptr) return MO_ERR_INVALID_ARG;
+    *out = make_layout(dims, precision).total;
+    return MO_OK;
+}
+
+int gather_muon_jobs(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, void* const* out,
+                     bool check_ptrs, std::vector<Job>& jobs, std::vector<int>* index_map) {
+    if (n < 0 || cfg == nullptr || (n > 0 && mats == nullptr)) return MO_ERR_INVALID_ARG;
+    if (cfg->ns_steps < 0 || (cfg->ns_precision != MO_NS_BF16 && cfg->ns_precision != MO_NS_FP32))
+        return MO_ERR_INVALID_ARG;
+    if (!cfg->apply_update && !valid_dtype(cfg->out_dtype)) return MO_ERR_INVALID_ARG;
+    if (check_ptrs && !cfg->apply_update && n > 0 && out == nullptr) return MO_ERR_INVALID_ARG;
+    jobs.clear();
+    for (int i = 0; i < n; ++i) {
+        const mo_matrix& mt = mats[i];
+        int st = validate_dims(mt.rows, mt.cols, mt.ld);
+        if (st != MO_OK) return st;
+        if (!valid_dtype(mt.w_dtype) || !valid_dtype(mt.m_dtype) || !valid_dtype(mt.g_dtype))
+            return MO_ERR_INVALID_ARG;
+        if (mt.rows == 0 || mt.cols == 0) continue;
+        if (check_ptrs) {
+            if ((st = validate_buffer(mt.M, mt.m_dtype, mt.ld)) != MO_OK) return st;
+            if ((st = validate_buffer(mt.G, mt.g_dtype, mt.ld)) != MO_OK) return st;
+            if (cfg->apply_update) {
+                if ((st = validate_buffer(mt.W, mt.w_dtype, mt.ld)) != MO_OK) return st;
+            } else {
+                if ((st = validate_buffer(out[i], cfg->out_dtype, mt.ld)) != MO_OK) return st;
+            }
+        }
+        Job j;
+        j.rows = mt.rows;
+        j.cols = mt.cols;
+        j.ld = mt.ld;
+        j.src_dtype = mt.m_dtype;
+        j.g_dtype = mt.g_dtype;
+        j.w_dtype = mt.w_dtype;
+        j.out_dtype = cfg->out_dtype;
+        j.has_momentum = 1;
+        j.src = mt.M;
+        j.grad = mt.G;
+        j.W = cfg->apply_update ? mt.W : nullptr;
+        j.out = (!cfg->apply_update && out) ? out[i] : nullptr;
+        jobs.push_back(j);
+        if (index_map) index_map->push_back(i);
+    }
+    return MO_OK;
+}
+
+}  // namespace
+}  // namespace mo
+
+using namespace mo;
+
+extern "C" {
+
+int mo_version(void) { return 0x000100; }
+
+const char* mo_status_string(int s) {
+    switch (s) {
+        case MO_OK: return "MO_OK";
+        case MO_ERR_INVALID_ARG: return "MO_ERR_INVALID_ARG: invalid argument";
+        case MO_ERR_ALIGNMENT: return "MO_ERR_ALIGNMENT: pointer or leading dimension not 16-byte aligned";
+        case MO_ERR_WORKSPACE: return "MO_ERR_WORKSPACE: workspace null, misaligned or too small";
+        case MO_ERR_CUDA: return "MO_ERR_CUDA: a CUDA call failed";
+        case MO_ERR_TIMEOUT: return "MO_ERR_TIMEOUT: a device-side wait gave up";
+        case MO_ERR_UNSUPPORTED: return "MO_ERR_UNSUPPORTED: outside what this build implements";
+        default: return "unknown status";
+    }
+}
+
+int mo_workspace_bytes(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, size_t* bytes_out) {
+    if (bytes_out == nullptr) return MO_ERR_INVALID_ARG;
+    std::vector<Job> jobs;
+    int st = gather_muon_jobs(mats, n, cfg, nullptr, false, jobs, nullptr);
+    if (st != MO_OK) return st;
+    std::vector<std::pair<int64_t, int64_t>> dims;
+    for (const Job& j : jobs) dims.push_back({j.rows, j.cols});
+    return ns_workspace_for(dims, cfg->ns_precision, bytes_out);
+}
+
+int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, const mo_adamw_tail* tail,
+                      void* const* out, void* ws, size_t ws_bytes, mo_stream_t stream) {
+    std::vector<Job> jobs;
+    int st = gather_muon_jobs(mats, n, cfg, out, true, jobs, nullptr);
+    if (st != MO_OK) return st;
+    if ((st = validate_tail(tail)) != MO_OK) return st;
+    if (!jobs.empty()) {
+        std::vector<std::pair<int64_t, int64_t>> dims;
+        for (const Job& j : jobs) dims.push_back({j.rows, j.cols});
+        size_t need = 0;
+        ns_workspace_for(dims, cfg->ns_precision, &need);
+        if ((st = validate_ws(ws, ws_bytes, need)) != MO_OK) return st;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (tail != nullptr && tail->numel > 0) {
+        if (launch_adamw(*tail, s) != cudaSuccess) return MO_ERR_CUDA;
+    }
+    NsOpts o;
+    o.precision = cfg->ns_precision;
+    o.steps = cfg->ns_steps;
+    o.apply_update = cfg->apply_update;
+    o.mu = cfg->mu;
+    o.a = cfg->a;
+    o.b = cfg->b;
+    o.c = cfg->c;
+    o.alpha = cfg->lr * cfg->update_scale;
+    o.decay = cfg->lr * cfg->weight_decay;
+    return run_ns(jobs, o, ws, ws_bytes, s);
+}
+
+int ns_workspace_bytes(const int64_t* rows, const int64_t* cols, int n, int precision, size_t* bytes_out) {
+    if (bytes_out == nullptr || n < 0 || (n > 0 && (rows == nullptr || cols == nullptr))) return MO_ERR_INVALID_ARG;
+    if (precision != MO_NS_BF16 && precision != MO_NS_FP32) return MO_ERR_INVALID_ARG;
+    std::vector<std::pair<int64_t, int64_t>> dims;
+    for (int i = 0; i < n; ++i) {
+        int st = validate_dims(rows[i], cols[i], cols[i]);
+        if (st != MO_OK) return st;
+        if (rows[i] > 0 && cols[i] > 0) dims.push_back({rows[i], cols[i]});
+    }
+    return ns_workspace_for(dims, precision, bytes_out);
+}
+
+int ns_orthogonalize(const void* const* X, void* const* out, const int64_t* rows, const int64_t* cols,
+                     const int64_t* ld, int n, int in_dtype, int out_dtype, int steps, float a, float b, float c,
+                     int precision, void* ws, size_t ws_bytes, mo_stream_t stream) {
+    if (n < 0 || steps < 0) return MO_ERR_INVALID_ARG;
+    if (precision != MO_NS_BF16 && precision != MO_NS_FP32) return MO_ERR_INVALID_ARG;
+    if (!valid_dtype(in_dtype) || !valid_dtype(out_dtype)) return MO_ERR_INVALID_ARG;
+    if (n > 0 && (!X || !out || !rows || !cols || !ld)) return MO_ERR_INVALID_ARG;
+    std::vector<Job> jobs;
+    for (int i = 0; i < n; ++i) {
+        int st = validate_dims(rows[i], cols[i], ld[i]);
+        if (st != MO_OK) return st;
+        if (rows[i] == 0 || cols[i] == 0) continue;
+        if ((st = validate_buffer(X[i], in_dtype, ld[i])) != MO_OK) return st;
+        if ((st = validate_buffer(out[i], out_dtype, ld[i])) != MO_OK) return st;
+        Job j;
+        j.rows = rows[i];
+        j.cols = cols[i];
+        j.ld = ld[i];
+        j.src_dtype = in_dtype;
+        j.g_dtype = in_dtype;
+        j.w_dtype = out_dtype;
+        j.out_dtype = out_dtype;
+        j.has_momentum = 0;
+        j.src = const_cast<void*>(X[i]);
+        j.grad = nullptr;
+        j.W = nullptr;
+        j.out = out[i];
+        jobs.push_back(j);
+    }
+    NsOpts o;
+    o.precision = precision;
+    o.steps = steps;
+    o.apply_update = 0;
+    o.mu = 0.f;
+    o.a = a;
+    o.b = b;
+    o.c = c;
+    o.alpha = 0.f;
+    o.decay = 0.f;
+    return run_ns(jobs, o, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, uint32_t* words,
+              mo_stream_t stream) {
+    if (!valid_dtype(dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (ld < cols || U == nullptr || words == nullptr) return MO_ERR_INVALID_ARG;
+    if (!aligned16(U) || (static_cast<size_t>(ld) * elem_size(dtype)) % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(words) & 3u) != 0)
+        return MO_ERR_ALIGNMENT;
+    return map_cuda(launch_sign_pack(U, dtype, rows, cols, ld, words, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols, void* W, int w_dtype,
+                     int64_t ld, float lr, mo_stream_t stream) {
+    if (M <= 0 || !valid_dtype(w_dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
+    if (M > 128) return MO_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (words == nullptr || W == nullptr || ld < cols) return MO_ERR_INVALID_ARG;
+    for (int m = 0; m < M; ++m) {
+        if (words[m] == nullptr) return MO_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(words[m]) & 3u) != 0) return MO_ERR_ALIGNMENT;
+    }
+    if (!aligned16(W) || (static_cast<size_t>(ld) * elem_size(w_dtype)) % 16 != 0) return MO_ERR_ALIGNMENT;
+    return map_cuda(launch_sign_vote_update(words, M, rows, cols, W, w_dtype, ld, lr,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int plan_owners(const int64_t* rows, const int64_t* cols, int n, int world, int ns_steps, double w_bytes,
+                double w_flops, int32_t* owner_out, double* load_out) {
+    if (world <= 0 || n < 0 || ns_steps < 0) return MO_ERR_INVALID_ARG;
+    if (n > 0 && (rows == nullptr || cols == nullptr || owner_out == nullptr)) return MO_ERR_INVALID_ARG;
+    std::vector<double> bytes(n), flops(n), cost(n);
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] < 0 || cols[i] < 0) return MO_ERR_INVALID_ARG;
+        const double r = static_cast<double>(rows[i]), c = static_cast<double>(cols[i]);
+        bytes[i] = r * c * 2.0;
+        const double m = rows[i] <= cols[i] ? r : c;
+        const double nn = rows[i] <= cols[i] ? c : r;
+        flops[i] = static_cast<double>(ns_steps) * (4.0 * m * m * nn + 2.0 * m * m * m);
+    }
+    double sb = 0.0, sf = 0.0;
+    for (int i = 0; i < n; ++i) sb += bytes[i];
+    for (int i = 0; i < n; ++i) sf += flops[i];
+    for (int i = 0; i < n; ++i) {
+        const double cb = sb > 0.0 ? bytes[i] / sb : 0.0;
+        const double cf = sf > 0.0 ? flops[i] / sf : 0.0;
+        const double tb = w_bytes * cb;
+        const double tf = w_flops * cf;
+        cost[i] = tb + tf;
+    }
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+        if (cost[x] != cost[y]) return cost[x] > cost[y];
+        return x < y;
+    });
+    std::vector<double> load(world, 0.0);
+    for (int i : order) {
+        int best = 0;
+        for (int r = 1; r < world; ++r)
+            if (load[r] < load[best]) best = r;
+        owner_out[i] = best;
+        load[best] += cost[i];
+    }
+    if (load_out != nullptr)
+        for (int r = 0; r < world; ++r) load_out[r] = load[r];
+    return MO_OK;
+}
+
+int mo_check_device_status(void* ws, mo_stream_t stream) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kWsAlign) != 0) return MO_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int err = 0;
+    if (cudaMemcpyAsync(&err, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MO_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MO_ERR_CUDA;
+    if (err != 0) {
+        const int zero = 0;
+        if (cudaMemcpyAsync(ws, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) return MO_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MO_ERR_CUDA;
+        return MO_ERR_TIMEOUT;
+    }
+    return MO_OK;
+}
+
+int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precision, int index,
+                     mo_ns_view* view) {
+    if (view == nullptr || n < 0 || index < 0 || index >= n || rows == nullptr || cols == nullptr)
+        return MO_ERR_INVALID_ARG;
+    if (precision != MO_NS_BF16 && precision != MO_NS_FP32) return MO_ERR_INVALID_ARG;
+    if (rows[index] <= 0 || cols[index] <= 0) return MO_ERR_INVALID_ARG;
+    std::vector<std::pair<int64_t, int64_t>> dims;
+    int active = -1;
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] > 0 && cols[i] > 0) {
+            if (i == index) active = static_cast<int>(dims.size());
+            dims.push_back({rows[i], cols[i]});
+        }
+    }
+    const Layout L = make_layout(dims, precision);
+    const Shape& s = L.shape[active];
+    const MatBufs& b = L.buf[active];
+    view->m = s.m;
+    view->n = s.n;
+    view->ldx = s.ldx;
+    view->lda = s.lda;
+    view->transposed = s.transposed;
+    view->precision = precision;
+    view->x_op[0] = static_cast<int64_t>(b.x_op[0]);
+    view->x_op[1] = static_cast<int64_t>(b.x_op[1]);
+    view->x_master = static_cast<int64_t>(b.x_master);
+    view->gram = static_cast<int64_t>(b.gram);
+    view->poly = static_cast<int64_t>(b.poly);
+    return MO_OK;
+}
+
+int mo_debug_sm_count(void) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return c;
+}
+
+int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo) {
+    // only the two readings of the MN-major 128-byte-swizzle layout; both keep
+    // every operand read inside the stage's 32 KB B buffer
+    const bool ok = (lbo == 8192u && sbo == 1024u) || (lbo == 1024u && sbo == 8192u);
+    if (!ok) return MO_ERR_INVALID_ARG;
+    g_mn_lbo.store(lbo);
+    g_mn_sbo.store(sbo);
+    return MO_OK;
+}
+
+}  // extern "C"

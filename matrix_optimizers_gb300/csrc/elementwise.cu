@@ -1,0 +1,430 @@
+// HBM-bound kernels of the Muon owner step:
+//   momentum_norm  M <- mu*M + G, per-tile sum of squares, NS operand written
+//                  in the oriented (m <= n) frame;
+//   norm_finalize  per-matrix 1/||X||_F and 1/||X||_F^2 from the tile sums;
+//   ns_k0          O = X/||X||_F applied directly when the step count is 0;
+//   sign_pack      sign -> 1 bit per element -> uint32 words (warp ballot);
+//   vote_update    popcount majority over M packed buffers fused with W -= lr*vote;
+//   adamw          vectorised AdamW on the flat float32 tail.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace mo {
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ float load_elem(const void* p, int dt, int64_t i) {
+    return dt == MO_F32 ? static_cast<const float*>(p)[i]
+                        : __bfloat162float(static_cast<const bf16*>(p)[i]);
+}
+__device__ __forceinline__ void store_elem(void* p, int dt, int64_t i, float v) {
+    if (dt == MO_F32)
+        static_cast<float*>(p)[i] = v;
+    else
+        static_cast<bf16*>(p)[i] = __float2bfloat16_rn(v);
+}
+// Loads up to 4 consecutive elements; a full group uses one vector access
+// (16-byte for f32, 8-byte for bf16; callers keep offsets 4-aligned).
+__device__ __forceinline__ void load4(const void* p, int dt, int64_t off, int nvalid, float v[4]) {
+    if (nvalid == 4) {
+        if (dt == MO_F32) {
+            float4 x = *reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        } else {
+            uint2 x = *reinterpret_cast<const uint2*>(static_cast<const bf16*>(p) + off);
+            __nv_bfloat162 lo = *reinterpret_cast<__nv_bfloat162*>(&x.x);
+            __nv_bfloat162 hi = *reinterpret_cast<__nv_bfloat162*>(&x.y);
+            v[0] = __low2float(lo); v[1] = __high2float(lo);
+            v[2] = __low2float(hi); v[3] = __high2float(hi);
+        }
+    } else {
+        for (int k = 0; k < 4; ++k) v[k] = k < nvalid ? load_elem(p, dt, off + k) : 0.f;
+    }
+}
+__device__ __forceinline__ void store4(void* p, int dt, int64_t off, int nvalid, const float v[4]) {
+    if (nvalid == 4) {
+        if (dt == MO_F32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(p) + off) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v[0], v[1]);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(v[2], v[3]);
+            uint2 x;
+            x.x = *reinterpret_cast<uint32_t*>(&lo);
+            x.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(static_cast<bf16*>(p) + off) = x;
+        }
+    } else {
+        for (int k = 0; k < nvalid; ++k) store_elem(p, dt, off + k, v[k]);
+    }
+}
+
+__device__ __forceinline__ int find_matrix(const MatDesc* mats, int nmats, int64_t t) {
+    int lo = 0, hi = nmats - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (mats[mid].mom_tile_begin <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.f;
+    if (threadIdx.x == 0)
+        for (int w = 0; w < 8; ++w) s += red[w];
+    __syncthreads();
+    return s;
+}
+
+// ------------------------------------------------------------ momentum_norm
+// Tile of 64 x 64 user elements per iteration, 256 threads: thread t owns
+// columns 4*(t%16)..+3 of rows t/16 + 16q, q = 0..3.
+__global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
+    __shared__ float tileT[kMomTile][kMomTile + 1];
+    __shared__ float red[8];
+    const int col4 = threadIdx.x & 15, rsub = threadIdx.x >> 4;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const MatDesc& md = p.mats[find_matrix(p.mats, p.nmats, t)];
+        const int64_t local = t - md.mom_tile_begin;
+        const int r0 = static_cast<int>(local / md.mom_tiles_c) * kMomTile;
+        const int c0 = static_cast<int>(local % md.mom_tiles_c) * kMomTile;
+        const int c = c0 + 4 * col4;
+        const int nvalid = max(0, min(4, md.cols - c));
+        const int op_dt = p.fp32_operand ? MO_F32 : MO_BF16;
+        float ss = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int rl = rsub + 16 * q, r = r0 + rl;
+            float x[4] = {0.f, 0.f, 0.f, 0.f};
+            if (r < md.rows && nvalid > 0) {
+                const int64_t off = static_cast<int64_t>(r) * md.ld + c;
+                float s[4];
+                load4(md.src, md.src_dtype, off, nvalid, s);
+                if (md.has_momentum) {
+                    float g[4];
+                    load4(md.grad, md.g_dtype, off, nvalid, g);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) x[k] = fmaf(p.mu, s[k], g[k]);
+                    if (md.src_dtype == MO_BF16) {   // stored momentum is the bf16 value
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) x[k] = __bfloat162float(__float2bfloat16_rn(x[k]));
+                    }
+                    store4(md.src, md.src_dtype, off, nvalid, x);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) x[k] = s[k];
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) ss = fmaf(x[k], x[k], ss);
+                if (!md.transposed)
+                    store4(md.x_op[0], op_dt, static_cast<int64_t>(r) * md.ldx + c, nvalid, x);
+            }
+            if (md.transposed) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) tileT[4 * col4 + k][rl] = x[k];
+            }
+        }
+        if (md.transposed) {
+            __syncthreads();
+            // oriented row xr = user column c0 + xr; oriented columns r0 + seg .. +15
+            const int xr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;
+            const int orow = c0 + xr;
+            if (orow < md.cols) {
+#pragma unroll
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    const int ocol = r0 + seg + 4 * g4;
+                    const int nv = max(0, min(4, md.rows - ocol));
+                    if (nv > 0) {
+                        float v[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) v[k] = tileT[xr][seg + 4 * g4 + k];
+                        store4(md.x_op[0], op_dt, static_cast<int64_t>(orow) * md.ldx + ocol, nv, v);
+                    }
+                }
+            }
+        }
+        const float total = block_sum_256(ss, red);   // also orders tileT reuse
+        if (threadIdx.x == 0) p.partials[t] = total;
+    }
+}
+
+cudaError_t launch_momentum_norm(const MomLaunch& p, int grid, cudaStream_t s) {
+    if (p.ntiles == 0) return cudaSuccess;
+    momentum_norm_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ norm_finalize
+// One warp per matrix sums its tile partials in a fixed order (float64).
+__global__ void __launch_bounds__(32) norm_finalize_kernel(const MatDesc* mats, const float* partials) {
+    const MatDesc& md = mats[blockIdx.x];
+    const int64_t nt = static_cast<int64_t>(md.mom_tiles_r) * md.mom_tiles_c;
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < nt; i += 32) s += static_cast<double>(partials[md.mom_tile_begin + i]);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (threadIdx.x == 0) {
+        float inv_s = 0.f, inv_s2 = 0.f;
+        if (s > 0.0) {
+            inv_s = static_cast<float>(1.0 / sqrt(s));
+            inv_s2 = static_cast<float>(1.0 / s);
+        }
+        md.scales[0] = inv_s;
+        md.scales[1] = inv_s2;
+    }
+}
+
+cudaError_t launch_norm_finalize(const MatDesc* mats, int nmats, const float* partials, cudaStream_t s) {
+    if (nmats == 0) return cudaSuccess;
+    norm_finalize_kernel<<<nmats, 32, 0, s>>>(mats, partials);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------- ns_k0
+// Zero Newton-Schulz steps: O = X / ||X||_F, elementwise in the user layout.
+struct K0Args {
+    MomLaunch p;
+    float alpha, decay;
+    int apply_update;
+};
+__global__ void __launch_bounds__(256) ns_k0_kernel(K0Args a) {
+    const MomLaunch& p = a.p;
+    const int col4 = threadIdx.x & 15, rsub = threadIdx.x >> 4;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const MatDesc& md = p.mats[find_matrix(p.mats, p.nmats, t)];
+        const int64_t local = t - md.mom_tile_begin;
+        const int r0 = static_cast<int>(local / md.mom_tiles_c) * kMomTile;
+        const int c0 = static_cast<int>(local % md.mom_tiles_c) * kMomTile;
+        const int c = c0 + 4 * col4;
+        const int nvalid = max(0, min(4, md.cols - c));
+        const float inv_s = md.scales[0];
+        for (int q = 0; q < 4; ++q) {
+            const int r = r0 + rsub + 16 * q;
+            if (r >= md.rows || nvalid <= 0) continue;
+            const int64_t off = static_cast<int64_t>(r) * md.ld + c;
+            float x[4];
+            load4(md.src, md.src_dtype, off, nvalid, x);
+            for (int k = 0; k < 4; ++k) x[k] *= inv_s;
+            if (a.apply_update) {
+                float w[4];
+                load4(md.W, md.w_dtype, off, nvalid, w);
+                for (int k = 0; k < 4; ++k) w[k] = fmaf(-a.alpha, x[k], w[k] - a.decay * w[k]);
+                store4(md.W, md.w_dtype, off, nvalid, w);
+            } else {
+                store4(md.out, md.out_dtype, off, nvalid, x);
+            }
+        }
+    }
+}
+
+cudaError_t launch_ns_k0(const MomLaunch& p, float alpha, float decay, int apply_update, int grid,
+                         cudaStream_t s) {
+    if (p.ntiles == 0) return cudaSuccess;
+    K0Args a{p, alpha, decay, apply_update};
+    ns_k0_kernel<<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+// --------------------------------------------------------------- sign_pack
+// One warp packs 16 consecutive words per iteration: lane l reads element
+// 32w + l of each word w and __ballot_sync assembles the word (bit l = lane l).
+constexpr int kPackWords = 16;
+
+template <typename T>
+__device__ __forceinline__ float to_float(T x);
+template <> __device__ __forceinline__ float to_float<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_float<bf16>(bf16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) sign_pack_kernel(const T* __restrict__ U, int64_t rows, int64_t cols,
+                                                        int64_t ld, uint32_t* __restrict__ words,
+                                                        int64_t nwords) {
+    const int lane = threadIdx.x & 31;
+    const int64_t numel = rows * cols;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t w0 = warp * kPackWords; w0 < nwords; w0 += nwarps * kPackWords) {
+        int64_t e = w0 * 32 + lane;
+        int64_t r = e / cols, c = e - r * cols;
+        float v[kPackWords];
+#pragma unroll
+        for (int q = 0; q < kPackWords; ++q) {
+            v[q] = 0.f;
+            if (e + 32 * q < numel) v[q] = to_float<T>(U[r * ld + c]);
+            c += 32;
+            while (c >= cols) { c -= cols; ++r; }
+        }
+        uint32_t mine = 0;
+#pragma unroll
+        for (int q = 0; q < kPackWords; ++q) {
+            const bool valid = (e + 32 * q) < numel;
+            const uint32_t word = __ballot_sync(0xffffffffu, valid && !(v[q] < 0.f));
+            if (lane == q) mine = word;
+        }
+        if (lane < kPackWords && w0 + lane < nwords) words[w0 + lane] = mine;
+    }
+}
+
+cudaError_t launch_sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                             uint32_t* words, cudaStream_t s) {
+    const int64_t nwords = (rows * cols + 31) / 32;
+    if (nwords == 0) return cudaSuccess;
+    const int64_t warps_needed = (nwords + kPackWords - 1) / kPackWords;
+    const int64_t blocks = (warps_needed + 7) / 8;
+    const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
+    if (dtype == MO_F32)
+        sign_pack_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(U), rows, cols, ld, words, nwords);
+    else
+        sign_pack_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(U), rows, cols, ld, words, nwords);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- vote_update
+// A warp takes 32 consecutive words: lane l reads word (base + l) of all M
+// buffers (coalesced), counts +1 votes per bit position with a bit-sliced
+// ripple counter, compares the count with ceil(M/2) bit-sliced, then the warp
+// updates the 1024 covered elements, 32 at a time (coalesced along W).
+constexpr int kMaxVoters = 128;
+struct VotePtrs {
+    const uint32_t* w[kMaxVoters];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) vote_update_kernel(const __grid_constant__ VotePtrs ptrs, int M, int nbits, uint32_t thr,
+                                                          int64_t rows, int64_t cols, int64_t ld,
+                                                          T* __restrict__ W, float lr, int64_t nwords) {
+    const int lane = threadIdx.x & 31;
+    const int64_t numel = rows * cols;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t base = warp * 32; base < nwords; base += nwarps * 32) {
+        const int64_t w = base + lane;
+        uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (w < nwords) {
+            for (int m = 0; m < M; ++m) {
+                uint32_t x = __ldg(ptrs.w[m] + w);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (j < nbits) {
+                        const uint32_t carry = cnt[j] & x;
+                        cnt[j] ^= x;
+                        x = carry;
+                    }
+                }
+            }
+        }
+        uint32_t gt = 0u, eq = 0xffffffffu;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            if (j < nbits) {
+                if ((thr >> j) & 1u) {
+                    eq &= cnt[j];
+                } else {
+                    gt |= eq & cnt[j];
+                    eq &= ~cnt[j];
+                }
+            }
+        }
+        const uint32_t plus = gt | eq;   // bit set: count >= ceil(M/2), i.e. vote +1
+        int64_t e = base * 32 + lane;
+        int64_t r = e / cols, c = e - r * cols;
+        for (int q = 0; q < 32; ++q) {
+            const uint32_t vw = __shfl_sync(0xffffffffu, plus, q);
+            if (e < numel) {
+                const int64_t idx = r * ld + c;
+                const float wv = to_float<T>(W[idx]);
+                const float nv = ((vw >> lane) & 1u) ? (wv - lr) : (wv + lr);
+                if constexpr (sizeof(T) == 4)
+                    W[idx] = nv;
+                else
+                    W[idx] = __float2bfloat16_rn(nv);
+            }
+            e += 32;
+            c += 32;
+            while (c >= cols) { c -= cols; ++r; }
+        }
+    }
+}
+
+cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols,
+                                    void* W, int w_dtype, int64_t ld, float lr, cudaStream_t s) {
+    const int64_t nwords = (rows * cols + 31) / 32;
+    if (nwords == 0) return cudaSuccess;
+    VotePtrs ptrs{};
+    for (int m = 0; m < M; ++m) ptrs.w[m] = words[m];
+    int nbits = 0;
+    while ((1 << nbits) <= M) ++nbits;
+    const uint32_t thr = static_cast<uint32_t>((M + 1) / 2);
+    const int64_t warps_needed = (nwords + 31) / 32;
+    const int64_t blocks = (warps_needed + 7) / 8;
+    const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
+    if (w_dtype == MO_F32)
+        vote_update_kernel<float><<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld,
+                                                       static_cast<float*>(W), lr, nwords);
+    else
+        vote_update_kernel<bf16><<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld,
+                                                      static_cast<bf16*>(W), lr, nwords);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------- adamw
+struct AdamArgs {
+    float* W; const float* g; float* m; float* v;
+    int64_t numel;
+    float beta1, beta2, eps, step_size, inv_bc2, decay;
+};
+
+__device__ __forceinline__ void adam_one(const AdamArgs& a, float& w, float g, float& m, float& v) {
+    m = fmaf(a.beta1, m, (1.f - a.beta1) * g);
+    v = fmaf(a.beta2, v, (1.f - a.beta2) * g * g);
+    const float denom = sqrtf(v * a.inv_bc2) + a.eps;
+    w = w - a.decay * w - a.step_size * (m / denom);
+}
+
+__global__ void __launch_bounds__(256) adamw_kernel(AdamArgs a) {
+    const int64_t n4 = a.numel >> 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+        float4 w = reinterpret_cast<float4*>(a.W)[i];
+        const float4 g = __ldcs(reinterpret_cast<const float4*>(a.g) + i);
+        float4 m = reinterpret_cast<float4*>(a.m)[i];
+        float4 v = reinterpret_cast<float4*>(a.v)[i];
+        adam_one(a, w.x, g.x, m.x, v.x);
+        adam_one(a, w.y, g.y, m.y, v.y);
+        adam_one(a, w.z, g.z, m.z, v.z);
+        adam_one(a, w.w, g.w, m.w, v.w);
+        reinterpret_cast<float4*>(a.W)[i] = w;
+        reinterpret_cast<float4*>(a.m)[i] = m;
+        reinterpret_cast<float4*>(a.v)[i] = v;
+    }
+    // scalar tail (numel % 4), handled by the first threads of block 0
+    if (blockIdx.x == 0 && threadIdx.x < (a.numel & 3)) {
+        const int64_t i = (n4 << 2) + threadIdx.x;
+        float w = a.W[i], m = a.m[i], v = a.v[i];
+        adam_one(a, w, a.g[i], m, v);
+        a.W[i] = w; a.m[i] = m; a.v[i] = v;
+    }
+}
+
+cudaError_t launch_adamw(const mo_adamw_tail& t, cudaStream_t s) {
+    if (t.numel == 0) return cudaSuccess;
+    AdamArgs a;
+    a.W = t.W; a.g = t.g; a.m = t.m; a.v = t.v; a.numel = t.numel;
+    a.beta1 = t.beta1; a.beta2 = t.beta2; a.eps = t.eps;
+    const double bc1 = 1.0 - pow(static_cast<double>(t.beta1), static_cast<double>(t.step));
+    const double bc2 = 1.0 - pow(static_cast<double>(t.beta2), static_cast<double>(t.step));
+    a.step_size = static_cast<float>(static_cast<double>(t.lr) / bc1);
+    a.inv_bc2 = static_cast<float>(1.0 / bc2);
+    a.decay = static_cast<float>(static_cast<double>(t.lr) * t.weight_decay);
+    const int64_t n4 = t.numel >> 2;
+    int64_t blocks = (n4 + 255) / 256;
+    const int64_t cap = device_sm_count() * 8LL;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    adamw_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace mo

@@ -1,0 +1,114 @@
+// Structures shared by the host orchestration and the kernels.  Plain
+// old data only: they are staged on the host and copied into the workspace.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/matrixopt.h"
+
+namespace mo {
+
+// Tile geometry of the tensor-core Newton-Schulz GEMM.
+constexpr int kTcBM = 128;   // rows of D per tile (TMEM lanes)
+constexpr int kTcBN = 256;   // columns of D per tile (TMEM columns per accumulator)
+constexpr int kTcBK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
+// Tile geometry of the CUDA-core fp32 GEMM.
+constexpr int kFpBM = 64, kFpBN = 64, kFpBK = 16;
+// Momentum / normalisation kernel tile.
+constexpr int kMomTile = 64;
+
+enum NsPhase : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
+
+// tcgen05 instruction descriptor of kind::f16: bf16 x bf16 -> f32, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t b_mn) {
+    return (1u << 4)            // D format f32
+           | (1u << 7)          // A format bf16
+           | (1u << 10)         // B format bf16
+           | (b_mn << 16)       // B major
+           | ((N >> 3) << 17)   // N / 8
+           | ((M >> 4) << 24);  // M / 16
+}
+
+// One matrix of the Newton-Schulz path, in the oriented frame: the NS
+// iterate X is m x n with m <= n; element (i, j) of X is element (i, j) of
+// the user matrix, or (j, i) when `transposed`.
+struct MatDesc {
+    int32_t m, n;              // oriented sizes
+    int32_t ldx, lda;          // workspace leading dims (elements) of X and of m x m buffers
+    int64_t ld;                // user leading dim (elements) of src / W / out / M / G
+    int32_t rows, cols;        // user sizes
+    int32_t transposed;
+    int32_t src_dtype;         // momentum / input dtype
+    int32_t g_dtype;           // gradient dtype (momentum kernel)
+    int32_t w_dtype;
+    int32_t out_dtype;
+    int32_t has_momentum;      // 1: src = M updated from G; 0: src = input X read only
+    void* src;                 // M (muon) or X (pure NS), user layout
+    const void* grad;          // G (muon) or null
+    void* W;                   // update target or null
+    void* out;                 // NS output target or null
+    void* x_op[2];             // NS operand ping-pong (bf16 or fp32), m x ldx
+    float* x_master;           // fp32 master of X (bf16 mode), m x ldx
+    void* gram;                // m x lda  (A = X X^T)
+    void* poly;                // m x lda  (B = b A + c A^2)
+    const CUtensorMap* tm_x[2];
+    const CUtensorMap* tm_gram;
+    const CUtensorMap* tm_poly;
+    float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix)
+    int64_t mom_tile_begin;    // first global index of this matrix's momentum tiles
+    int32_t mom_tiles_r, mom_tiles_c;
+};
+
+// One tile of a grouped GEMM phase.
+struct TileDesc {
+    int32_t mat;       // matrix index
+    int32_t ti, tj;    // tile row / column index
+    int32_t nkb;       // K blocks
+};
+
+struct NsLaunch {
+    const MatDesc* mats;
+    const TileDesc* tiles;
+    const int2* cta_range;     // per CTA {first tile, tile count} (tensor-core path)
+    int* err;
+    int32_t phase, step, steps;
+    int32_t apply_update;
+    float a, b, c;
+    float alpha;               // lr * update_scale
+    float decay;               // lr * weight_decay
+    uint32_t idesc;
+    uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
+    int32_t ntiles;
+};
+
+struct MomLaunch {
+    const MatDesc* mats;
+    int32_t nmats;
+    int64_t ntiles;
+    float mu;
+    int32_t fp32_operand;      // write the fp32 operand (fp32 NS) instead of bf16
+    float* partials;           // one fp32 sum of squares per momentum tile
+};
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_momentum_norm(const MomLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_norm_finalize(const MatDesc* mats, int nmats, const float* partials,
+                                 cudaStream_t s);
+cudaError_t launch_ns_k0(const MomLaunch& p, float alpha, float decay, int apply_update, int grid,
+                         cudaStream_t s);
+cudaError_t launch_ns_tc_phase(const NsLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_ns_fp32_phase(const NsLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                             uint32_t* words, cudaStream_t s);
+cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t rows,
+                                    int64_t cols, void* W, int w_dtype, int64_t ld, float lr,
+                                    cudaStream_t s);
+cudaError_t launch_adamw(const mo_adamw_tail& t, cudaStream_t s);
+
+int tc_smem_bytes();
+int device_sm_count();
+
+}  // namespace mo

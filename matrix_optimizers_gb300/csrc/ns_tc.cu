@@ -1,0 +1,408 @@
+// Grouped tensor-core GEMM for the quintic Newton-Schulz step on sm_103a.
+//
+// One persistent launch per phase covers every matrix of the batch:
+//   kGram   A = s * X X^T          (X: m x n bf16, K = n; s = 1/||M||_F^2 at step 0)
+//   kPoly   B = b*A + c * A A      (K = m; A is symmetric so A A = A A^T)
+//   kApply  X' = a*X + B X         (K = m; step 0: X' = (a*M + B Xb)/||M||_F)
+//           the last step writes W <- W - lr*wd*W - lr*scale*X' (or the output)
+// kGram and kPoly compute only the 128 x 256 tiles that meet the upper
+// triangle (j >= i) and store each upper element at (i, j) and (j, i).
+//
+// Roles per CTA (320 threads, one CTA per SM):
+//   warps 0-7  epilogue: tcgen05.ld of the fp32 accumulator, fused math,
+//              global stores; warp w reads TMEM lanes 32*(w%4).. and column
+//              half w/4 of the 256-column accumulator;
+//   warp 8     TMA producer: 64 x 64 bf16 boxes (128-byte swizzle) into a
+//              4-stage shared-memory ring (48 KB per stage);
+//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
+//              (M = 128, N = 256, K = 16 per instruction) into a double-
+//              buffered accumulator (2 x 256 TMEM columns), so the epilogue
+//              of one tile overlaps the main loop of the next.
+// Every barrier wait is bounded (see ptx.cuh); a timeout raises the CTA's
+// abort flag, records an error code and unwinds after draining copies.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mo {
+
+using bf16 = __nv_bfloat16;
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBox = 64;                                   // TMA box edge (elements)
+constexpr int kBoxBytes = kBox * kBox * 2;                 // 8 KB
+constexpr int kABytes = kTcBM * kTcBK * 2;                 // 16 KB
+constexpr int kBBytes = kTcBN * kTcBK * 2;                 // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr uint32_t kTmemCols = 512;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+
+struct Ctl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// ---------------------------------------------------------------- helpers
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = __low2float(h[q]);
+        v[2 * q + 1] = __high2float(h[q]);
+    }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+        w[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return u;
+}
+
+// 32 consecutive elements starting at p[off]; `nv` of them valid.  A full
+// group is read with 16-byte vector loads (offsets are 32-element aligned
+// and leading dimensions 16-byte multiples).
+__device__ __forceinline__ void load32(const void* p, int dt, int64_t off, int nv, float (&v)[32]) {
+    if (nv == 32) {
+        if (dt == MO_F32) {
+            const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = s[q];
+                v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+            }
+        } else {
+            const uint4* s = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) unpack_bf16x8(s[q], &v[8 * q]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            float x = 0.f;
+            if (k < nv)
+                x = dt == MO_F32 ? static_cast<const float*>(p)[off + k]
+                                 : __bfloat162float(static_cast<const bf16*>(p)[off + k]);
+            v[k] = x;
+        }
+    }
+}
+__device__ __forceinline__ void store32(void* p, int dt, int64_t off, int nv, const float (&v)[32]) {
+    if (nv == 32) {
+        if (dt == MO_F32) {
+            float4* d = reinterpret_cast<float4*>(static_cast<float*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+            uint4* d = reinterpret_cast<uint4*>(static_cast<bf16*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[q] = pack_bf16x8(&v[8 * q]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (k < nv) {
+                if (dt == MO_F32)
+                    static_cast<float*>(p)[off + k] = v[k];
+                else
+                    static_cast<bf16*>(p)[off + k] = __float2bfloat16_rn(v[k]);
+            }
+        }
+    }
+}
+__device__ __forceinline__ float load1(const void* p, int dt, int64_t off) {
+    return dt == MO_F32 ? static_cast<const float*>(p)[off] : __bfloat162float(static_cast<const bf16*>(p)[off]);
+}
+__device__ __forceinline__ void store1(void* p, int dt, int64_t off, float v) {
+    if (dt == MO_F32)
+        static_cast<float*>(p)[off] = v;
+    else
+        static_cast<bf16*>(p)[off] = __float2bfloat16_rn(v);
+}
+
+// Oriented access to a user matrix: X(i, j) = U(i, j), or U(j, i) when the
+// matrix was transposed to reach m <= n.  Transposed accesses are per
+// element; across a warp (consecutive i) they are contiguous.
+__device__ __forceinline__ void user_load32(const MatDesc& md, const void* p, int dt, int i, int j0, int nv,
+                                            float (&v)[32]) {
+    if (!md.transposed) {
+        load32(p, dt, static_cast<int64_t>(i) * md.ld + j0, nv, v);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = k < nv ? load1(p, dt, static_cast<int64_t>(j0 + k) * md.ld + i) : 0.f;
+    }
+}
+__device__ __forceinline__ void user_store32(const MatDesc& md, void* p, int dt, int i, int j0, int nv,
+                                             const float (&v)[32]) {
+    if (!md.transposed) {
+        store32(p, dt, static_cast<int64_t>(i) * md.ld + j0, nv, v);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < nv) store1(p, dt, static_cast<int64_t>(j0 + k) * md.ld + i, v[k]);
+    }
+}
+
+// ------------------------------------------------------------- epilogues
+// Symmetric phases: keep elements with j >= i, store at (i, j) and (j, i).
+__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int i, int j0,
+                                              float (&v)[32]) {
+    const int m = md.m;
+    if (j0 + 31 < i || j0 >= m) return;
+    bf16* dst = static_cast<bf16*>(p.phase == kGram ? md.gram : md.poly);
+    const int nv = min(32, m - j0);
+    if (p.phase == kGram) {
+        const float sc = p.step == 0 ? md.scales[1] : 1.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] *= sc;
+    } else {
+        float a[32];
+        load32(md.gram, MO_BF16, static_cast<int64_t>(i) * md.lda + j0, nv, a);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = fmaf(p.c, v[k], p.b * a[k]);
+    }
+    const int64_t row = static_cast<int64_t>(i) * md.lda;
+    if (j0 >= i) {
+        store32(dst, MO_BF16, row + j0, nv, v);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (j0 + k >= i && k < nv) dst[row + j0 + k] = __float2bfloat16_rn(v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int j = j0 + k;
+        if (j > i && k < nv) dst[static_cast<int64_t>(j) * md.lda + i] = __float2bfloat16_rn(v[k]);
+    }
+}
+
+__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int i, int j0,
+                                          float (&v)[32]) {
+    const int n = md.n;
+    if (j0 >= n) return;
+    const int nv = min(32, n - j0);
+    float x[32];
+    if (p.step == 0) {
+        user_load32(md, md.src, md.src_dtype, i, j0, nv, x);
+        const float inv_s = md.scales[0];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
+    } else {
+        load32(md.x_master, MO_F32, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
+    }
+    if (p.step + 1 < p.steps) {
+        const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
+        store32(md.x_master, MO_F32, off, nv, x);
+        store32(md.x_op[(p.step + 1) & 1], MO_BF16, off, nv, x);
+        return;
+    }
+    if (p.apply_update) {
+        if (md.W == nullptr) return;
+        float w[32];
+        user_load32(md, md.W, md.w_dtype, i, j0, nv, w);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w[k] = fmaf(-p.alpha, x[k], w[k] - p.decay * w[k]);
+        user_store32(md, md.W, md.w_dtype, i, j0, nv, w);
+    } else if (md.out != nullptr) {
+        user_store32(md, md.out, md.out_dtype, i, j0, nv, x);
+    }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constant__ NsLaunch p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tfull[a]), 1);
+            mbar_init(smem_u32(&ctl->tempty[a]), kEpiWarps);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int* abort_flag = &ctl->abort_flag;
+    const int2 range = p.cta_range[blockIdx.x];
+    const bool mn_b = p.phase == kApply;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed[kStages] = {0, 0, 0, 0};
+            bool ok = true;
+            for (int t = 0; t < range.y && ok; ++t) {
+                const TileDesc td = p.tiles[range.x + t];
+                const MatDesc& md = p.mats[td.mat];
+                const int i0 = td.ti * kTcBM, j0 = td.tj * kTcBN;
+                const CUtensorMap* tma;
+                const CUtensorMap* tmb;
+                if (p.phase == kGram) {
+                    tma = tmb = md.tm_x[p.step & 1];
+                } else if (p.phase == kPoly) {
+                    tma = tmb = md.tm_gram;
+                } else {
+                    tma = md.tm_poly;
+                    tmb = md.tm_x[p.step & 1];
+                }
+                for (int kb = 0; kb < td.nkb; ++kb) {
+                    const uint32_t empty = smem_u32(&ctl->empty[stage]);
+                    const uint32_t full = smem_u32(&ctl->full[stage]);
+                    if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) { ok = false; break; }
+                    mbar_arrive_expect_tx(full, kStageBytes);
+                    ++armed[stage];
+                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    const int k0 = kb * kTcBK;
+                    tma_load_2d(sa, tma, full, k0, i0);
+                    tma_load_2d(sa + kBoxBytes, tma, full, k0, i0 + kBox);
+                    if (!mn_b) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, k0, j0 + q * kBox);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, j0 + q * kBox, k0);
+                    }
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let every armed copy land before the CTA exits
+                for (int s = 0; s < kStages; ++s) {
+                    if (armed[s] == 0) continue;
+                    const uint32_t full = smem_u32(&ctl->full[s]);
+                    const uint32_t par = (armed[s] - 1u) & 1u;
+                    long long t0 = clock64();
+                    while (!mbar_try_wait(full, par) && clock64() - t0 < kWaitCycles) {}
+                }
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = 0; t < range.y && ok; ++t) {
+                const TileDesc td = p.tiles[range.x + t];
+                const int acc = t & 1;
+                const uint32_t acc_phase = (t >> 1) & 1;
+                if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, abort_flag, p.err, 0x102)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + static_cast<uint32_t>(acc * kTcBN);
+                for (int kb = 0; kb < td.nkb; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, p.err, 0x103)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+#pragma unroll
+                    for (int k = 0; k < kTcBK / 16; ++k) {
+                        const uint64_t ad = sdesc_sw128(sa + k * 32, 16, 1024);
+                        const uint64_t bd = mn_b ? sdesc_sw128(sb + k * 16 * 128, p.mn_lbo, p.mn_sbo)
+                                                 : sdesc_sw128(sb + k * 32, 16, 1024);
+                        umma_bf16(d, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&ctl->empty[stage]));
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit(smem_u32(&ctl->tfull[acc]));
+            }
+            // all issued MMAs complete before TMEM is released
+            umma_commit(smem_u32(&ctl->drain));
+            long long t0 = clock64();
+            while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < kWaitCycles) {}
+        }
+    } else {
+        const int quarter = warp & 3, half = warp >> 2;
+        for (int t = 0; t < range.y; ++t) {
+            const TileDesc td = p.tiles[range.x + t];
+            const MatDesc& md = p.mats[td.mat];
+            const int acc = t & 1;
+            const uint32_t acc_phase = (t >> 1) & 1;
+            if (!mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104)) break;
+            tc_fence_after();
+            const int i = td.ti * kTcBM + quarter * 32 + lane;
+            const bool row_ok = i < md.m;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                const int col = half * 128 + ch * 32;
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(acc * kTcBN + col),
+                                   r);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                float v[32];
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+                const int j0 = td.tj * kTcBN + col;
+                if (p.phase == kApply)
+                    epi_apply(p, md, i, j0, v);
+                else
+                    epi_symmetric(p, md, i, j0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_ns_tc_phase(const NsLaunch& p, int grid, cudaStream_t s) {
+    if (grid <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    ns_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace mo

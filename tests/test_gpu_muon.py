@@ -1,0 +1,197 @@
+"""GPU parity of the whole Muon step (muon_step_batched) on the workloads:
+momentum, NS, update and the AdamW tail, against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import matrix_optimizers_gb300 as mo
+from oracle import adamw as oa
+from oracle import muon as om
+from oracle import planner as oplan
+from oracle import sign as osg
+from tests.gpu_helpers import MOM_TOL, NS_BF16_TOL, NS_FP32_TOL, dev, rel_fro, to_dev, to_np, workspace
+from workloads import (CONFIGS, llama7b_shapes, matrix_inputs, matrix_set_inputs, ragged_shapes,
+                       sign_muon_inputs,
+                       single_matrix_inputs, tail_inputs)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(inputs, cfg, tail=None, out=None, m_dtype=torch.float32):
+    Ws = [to_dev(x["W"]) for x in inputs]
+    Ms = [to_dev(x["M0"], m_dtype) if "M0" in x else
+          torch.zeros(x["W"].shape, dtype=m_dtype, device=dev()) for x in inputs]
+    Gs = [to_dev(x["G"]) for x in inputs]
+    mats = [mo.make_matrix(w, m, g) for w, m, g in zip(Ws, Ms, Gs)]
+    ws = workspace(mo.mo_workspace_bytes(mats, cfg))
+    mo.muon_step_batched(mats, cfg, ws, tail=tail, out=out)
+    torch.cuda.synchronize()
+    assert mo.mo_check_device_status(ws) == 0
+    return Ws, Ms
+
+
+def _check_update(W_gpu, inp, mu, lr, tol, m_dtype="f32"):
+    W0 = inp["W"].astype(np.float64)
+    M0 = inp["M0"].astype(np.float64) if "M0" in inp else np.zeros_like(W0)
+    Wn, _, _ = om.muon_step(W0, M0, inp["G"].astype(np.float64), mu=mu, lr=lr, m_dtype=m_dtype)
+    err = rel_fro(to_np(W_gpu) - W0, Wn - W0)
+    assert err < tol, err
+    return err
+
+
+def test_single_256x512_fp32_mode():
+    cfg_d = CONFIGS["single_256x512"]
+    inp = single_matrix_inputs()
+    cfg = mo.make_cfg(mu=cfg_d["mu"], lr=cfg_d["lr"], precision=mo.MO_NS_FP32)
+    Ws, Ms = _run([inp], cfg)
+    M1 = om.momentum(inp["M0"], inp["G"], cfg_d["mu"])
+    assert rel_fro(to_np(Ms[0]), M1) < MOM_TOL
+    _check_update(Ws[0], inp, cfg_d["mu"], cfg_d["lr"], NS_FP32_TOL)
+
+
+def test_single_256x512_bf16_mode():
+    inp = single_matrix_inputs()
+    cfg = mo.make_cfg(mu=0.95, lr=0.02)
+    Ws, _ = _run([inp], cfg)
+    _check_update(Ws[0], inp, 0.95, 0.02, NS_BF16_TOL)
+
+
+def test_gpt_small_full_step_with_tail():
+    c = CONFIGS["gpt_small"]
+    shapes = c["shapes"]
+    inputs = [matrix_inputs(shapes, i) for i in range(len(shapes))]
+    # a second step with non-zero momentum: run step 1 on the oracle for M0
+    for inp in inputs:
+        inp["M0"] = (0.5 * inp["G"]).astype(np.float32)
+    t = tail_inputs(c["tail_numel"])
+    tW, tg, tm_, tv = (torch.from_numpy(t[k]).to(dev()) for k in ("W", "g", "m", "v"))
+    tail = mo.make_tail(tW, tg, tm_, tv, step=1, lr=c["tail_lr"])
+    cfg = mo.make_cfg(mu=c["mu"], lr=c["lr"])
+    Ws, Ms = _run(inputs, cfg, tail=tail)
+    worst = 0.0
+    for i, inp in enumerate(inputs):
+        M1 = om.momentum(inp["M0"], inp["G"], c["mu"])
+        assert rel_fro(to_np(Ms[i]), M1) < MOM_TOL
+        worst = max(worst, _check_update(Ws[i], inp, c["mu"], c["lr"], NS_BF16_TOL))
+    Wt, _, _ = oa.adamw_step(t["W"], t["g"], t["m"], t["v"], 1, lr=c["tail_lr"])
+    assert np.max(np.abs(tW.cpu().numpy() - Wt)) < 1e-8
+
+
+def test_weight_decay_and_update_scale():
+    rng = np.random.default_rng(9)
+    inp = {"W": rng.standard_normal((128, 384)).astype(np.float32),
+           "G": rng.standard_normal((128, 384)).astype(np.float32),
+           "M0": rng.standard_normal((128, 384)).astype(np.float32)}
+    cfg = mo.make_cfg(mu=0.9, lr=0.05, update_scale=1.7, weight_decay=0.2)
+    Ws, _ = _run([inp], cfg)
+    W0 = inp["W"].astype(np.float64)
+    Wn, _, _ = om.muon_step(W0, inp["M0"], inp["G"], mu=0.9, lr=0.05, update_scale=1.7, weight_decay=0.2)
+    assert rel_fro(to_np(Ws[0]) - W0, Wn - W0) < NS_BF16_TOL
+
+
+def test_bf16_state_dtypes():
+    rng = np.random.default_rng(10)
+    inp = {"W": rng.standard_normal((192, 256)).astype(np.float32),
+           "G": rng.standard_normal((192, 256)).astype(np.float32),
+           "M0": rng.standard_normal((192, 256)).astype(np.float32)}
+    W = to_dev(inp["W"], torch.bfloat16)
+    M = to_dev(inp["M0"], torch.bfloat16)
+    G = to_dev(inp["G"], torch.bfloat16)
+    W0, M0, G0 = to_np(W), to_np(M), to_np(G)
+    mats = [mo.make_matrix(W, M, G)]
+    cfg = mo.make_cfg(mu=0.95, lr=0.05)
+    ws = workspace(mo.mo_workspace_bytes(mats, cfg))
+    mo.muon_step_batched(mats, cfg, ws)
+    torch.cuda.synchronize()
+    Wn, Mn, _ = om.muon_step(W0, M0, G0, mu=0.95, lr=0.05, m_dtype="bf16")
+    # W is stored in bf16: compare the update with bf16 storage noise allowed
+    assert rel_fro(to_np(W) - W0, Wn - W0) < 3e-2
+    assert rel_fro(to_np(M), Mn) < 4e-3
+
+
+def test_apply_update_off_writes_output():
+    rng = np.random.default_rng(11)
+    shapes = [(256, 384), (384, 256)]
+    inputs = [{"W": np.zeros(s, np.float32), "G": rng.standard_normal(s).astype(np.float32),
+               "M0": np.zeros(s, np.float32)} for s in shapes]
+    outs = [torch.zeros(s, dtype=torch.bfloat16, device=dev()) for s in shapes]
+    cfg = mo.make_cfg(mu=0.95, lr=0.02, apply_update=False, out_dtype=mo.MO_BF16)
+    Ws, _ = _run(inputs, cfg, out=outs)
+    for inp, o, w in zip(inputs, outs, Ws):
+        assert torch.all(w == 0)
+        want = om.newton_schulz(om.momentum(inp["M0"], inp["G"], 0.95))
+        assert rel_fro(to_np(o), want) < NS_BF16_TOL
+
+
+def test_sign_muon_m8_step_bit_exact_vote():
+    c = CONFIGS["sign_muon_m8"]
+    inp = sign_muon_inputs()
+    n = 2048
+    Ms = [torch.zeros(n, n, dtype=torch.bfloat16, device=dev()) for _ in range(8)]
+    Gs = [torch.from_numpy(g).to(dev()) for g in inp["G"]]
+    dummyW = [torch.zeros(1, dtype=torch.float32, device=dev()) for _ in range(8)]
+    U = [torch.zeros(n, n, dtype=torch.bfloat16, device=dev()) for _ in range(8)]
+    mats = [mo.make_matrix(M, M, G) for M, G in zip(Ms, Gs)]      # W unused without update
+    cfg = mo.make_cfg(mu=c["mu"], lr=c["lr"], apply_update=False, out_dtype=mo.MO_BF16)
+    ws = workspace(mo.mo_workspace_bytes(mats, cfg))
+    mo.muon_step_batched(mats, cfg, ws, out=U)
+    words = [torch.empty((n * n + 31) // 32, dtype=torch.int32, device=dev()) for _ in range(8)]
+    for u, w in zip(U, words):
+        mo.sign_pack(u, w)
+    W = torch.from_numpy(inp["W"]).to(dev())
+    W0 = inp["W"].astype(np.float64)
+    mo.sign_vote_update(words, W, c["lr"])
+    torch.cuda.synchronize()
+    del dummyW
+    # NS outputs vs the oracle (momentum stored in bf16)
+    for m in (0, 5):
+        _, Mst, O = om.muon_step(np.zeros((n, n)), np.zeros((n, n)), inp["G"][m], mu=c["mu"], lr=c["lr"],
+                                 m_dtype="bf16", apply_update=False)
+        assert rel_fro(to_np(Ms[m]), Mst) < 1e-7
+        assert rel_fro(to_np(U[m]), O) < NS_BF16_TOL
+    # pack and vote: bit-exact on the GPU's own sign buffers
+    ref_words = [osg.pack_bits(to_np(u)) for u in U]
+    for w, r in zip(words, ref_words):
+        assert np.array_equal(w.cpu().numpy().view(np.uint32), r)
+    assert np.array_equal(to_np(W), osg.vote_update(W0, ref_words, c["lr"]))
+
+
+@pytest.mark.slow
+def test_llama7b_owner0_sampled():
+    c = CONFIGS["llama7b_owner0"]
+    shapes = llama7b_shapes()
+    owner, _ = oplan.plan_owners(shapes, 8, 5)
+    mine = [i for i in range(len(shapes)) if owner[i] == 0]
+    assert len(mine) == 28
+    inputs = matrix_set_inputs(shapes, mine)
+    cfg = mo.make_cfg(mu=c["mu"], lr=c["lr"])
+    Ws, Ms = _run(inputs, cfg)
+    sq = next(k for k, i in enumerate(mine) if shapes[i][0] == shapes[i][1])
+    rect = next(k for k, i in enumerate(mine) if shapes[i][0] > shapes[i][1])
+    for k in (sq, rect):
+        _check_update(Ws[k], inputs[k], c["mu"], c["lr"], NS_BF16_TOL)
+    # every matrix: the update is finite and its Frobenius norm lies in the
+    # NS band: ||O||_F^2 = sum sigma_i^2 with each sigma in [0.68, 1.21]
+    for k, i in enumerate(mine):
+        d = (to_np(Ws[k]) - inputs[k]["W"]) / c["lr"]
+        m = min(shapes[i])
+        f2 = float(np.sum(d * d)) / m
+        assert np.isfinite(f2) and 0.68 ** 2 * 0.95 < f2 < 1.21 ** 2 * 1.05
+        assert rel_fro(to_np(Ms[k]), inputs[k]["G"]) < MOM_TOL
+
+
+@pytest.mark.slow
+def test_ragged500_sampled():
+    c = CONFIGS["ragged500"]
+    shapes = ragged_shapes()
+    inputs = matrix_set_inputs(shapes)
+    cfg = mo.make_cfg(mu=c["mu"], lr=c["lr"])
+    Ws, _ = _run(inputs, cfg)
+    sizes = [r * cc for r, cc in shapes]
+    picks = {int(np.argmin(sizes)), int(np.argmax([min(s) for s in shapes])), 17, 250, 499}
+    picks = [k for k in picks if min(shapes[k]) <= 4096]
+    for k in picks:
+        _check_update(Ws[k], inputs[k], c["mu"], c["lr"], NS_BF16_TOL)
+    for k in range(len(shapes)):
+        d = (to_np(Ws[k]) - inputs[k]["W"]) / c["lr"]
+        assert np.all(np.isfinite(d))

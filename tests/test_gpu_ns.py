@@ -1,0 +1,138 @@
+"""GPU parity of the Newton-Schulz path through the C ABI: each phase alone
+(via the workspace view), ns_orthogonalize in bf16 and fp32 modes, the
+degenerate cases, and the invariances the oracle is pinned to."""
+import numpy as np
+import pytest
+import torch
+
+import matrix_optimizers_gb300 as mo
+from matrix_optimizers_gb300 import _binding as B
+from oracle import bf16 as ob
+from oracle import muon as om
+from tests.gpu_helpers import NS_BF16_TOL, NS_FP32_TOL, dev, rel_fro, to_dev, to_np, workspace, ws_view
+
+pytestmark = pytest.mark.gpu
+
+A, Bc, C = om.NS_A, om.NS_B, om.NS_C
+
+
+def _ns(X_list, steps=5, precision=mo.MO_NS_BF16, out_dtype=torch.float32, coeffs=(A, Bc, C), lds=None):
+    shapes = [tuple(x.shape) for x in X_list]
+    ws = workspace(mo.ns_workspace_bytes(shapes, precision))
+    lds = lds or [None] * len(X_list)
+    Xt = [to_dev(x, torch.float32, ld) for x, ld in zip(X_list, lds)]
+    outs = []
+    for x, ld in zip(X_list, lds):
+        o = to_dev(np.zeros(x.shape), out_dtype, ld)
+        outs.append(o)
+    mo.ns_orthogonalize(Xt, outs, steps, ws, *coeffs, precision=precision)
+    torch.cuda.synchronize()
+    assert mo.mo_check_device_status(ws) == 0
+    return [to_np(o) for o in outs], ws, Xt
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (128, 256), (200, 300), (300, 200), (64, 64)])
+def test_phases_individually(shape):
+    """steps = 1: the Gram, polynomial and apply buffers each match the oracle
+    computed from the bf16 operands the kernels used."""
+    X = np.random.default_rng(1).standard_normal(shape)
+    outs, ws, _ = _ns([X], steps=1)
+    v = B.mo_debug_ns_view([shape], 0)
+    m, n = v.m, v.n
+    Xo = X.T if v.transposed else X
+    s = np.linalg.norm(Xo.astype(np.float32).astype(np.float64))
+    Xb = ob.round_bf16(Xo.astype(np.float32).astype(np.float64))        # operand the kernels read
+    xb_dev = to_np(ws_view(ws, v.x_op[0], (m, n), torch.bfloat16, v.ldx))
+    assert np.array_equal(xb_dev, Xb)
+    gram = to_np(ws_view(ws, v.gram, (m, m), torch.bfloat16, v.lda))
+    want_gram = Xb @ Xb.T / s ** 2
+    assert rel_fro(gram, want_gram) < 4e-3                                # bf16 storage of A
+    assert np.array_equal(gram, gram.T)                                   # mirrored exactly
+    poly = to_np(ws_view(ws, v.poly, (m, m), torch.bfloat16, v.lda))
+    want_poly = Bc * gram + C * gram @ gram
+    assert rel_fro(poly, want_poly) < 4e-3
+    assert np.array_equal(poly, poly.T)
+    want_x1 = (A * Xo.astype(np.float32) + poly @ Xb) / s
+    got = outs[0].T if v.transposed else outs[0]
+    assert rel_fro(got, want_x1) < 1e-5
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (768, 768), (768, 3072), (3072, 768), (100, 300),
+                                   (300, 100), (64, 64), (8, 40), (1, 33), (200, 1000), (1000, 200),
+                                   (520, 1032), (136, 2056)])
+def test_ns_bf16_vs_oracle(shape):
+    X = np.random.default_rng(sum(shape)).standard_normal(shape)
+    got = _ns([X])[0][0]
+    want = om.newton_schulz(X.astype(np.float32).astype(np.float64))
+    assert rel_fro(got, want) < NS_BF16_TOL
+
+
+def test_ns_bf16_batch_mixed_shapes_and_ld():
+    rng = np.random.default_rng(7)
+    shapes = [(256, 512), (512, 256), (96, 160), (384, 384), (72, 576)]
+    lds = [520, 264, 168, None, 584]
+    X = [rng.standard_normal(s) for s in shapes]
+    outs, _, _ = _ns(X, lds=lds)
+    for x, o in zip(X, outs):
+        assert rel_fro(o, om.newton_schulz(x.astype(np.float32).astype(np.float64))) < NS_BF16_TOL
+
+
+@pytest.mark.parametrize("shape", [(256, 512), (300, 200), (64, 64), (130, 70), (1, 9)])
+def test_ns_fp32_vs_oracle(shape):
+    X = np.random.default_rng(sum(shape) + 1).standard_normal(shape)
+    got = _ns([X], precision=mo.MO_NS_FP32)[0][0]
+    want = om.newton_schulz(X.astype(np.float32).astype(np.float64))
+    assert rel_fro(got, want) < NS_FP32_TOL
+
+
+@pytest.mark.parametrize("precision", [mo.MO_NS_BF16, mo.MO_NS_FP32])
+def test_ns_degenerate(precision):
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((96, 200))
+    got0 = _ns([X], steps=0, precision=precision)[0][0]
+    x32 = X.astype(np.float32).astype(np.float64)
+    assert rel_fro(got0, x32 / np.linalg.norm(x32)) < 1e-6
+    Z = np.zeros((64, 128))
+    assert np.all(_ns([Z], precision=precision)[0][0] == 0)
+    ident = _ns([X], steps=3, precision=precision, coeffs=(1.0, 0.0, 0.0))[0][0]
+    assert rel_fro(ident, x32 / np.linalg.norm(x32)) < (3e-3 if precision == mo.MO_NS_BF16 else 1e-6)
+
+
+@pytest.mark.parametrize("precision", [mo.MO_NS_BF16, mo.MO_NS_FP32])
+def test_ns_power_of_two_scale_is_bitwise(precision):
+    X = np.random.default_rng(4).standard_normal((192, 320))
+    a = _ns([X], precision=precision)[0][0]
+    b = _ns([X * 2.0 ** 5], precision=precision)[0][0]
+    c = _ns([X * 2.0 ** -9], precision=precision)[0][0]
+    assert np.array_equal(a, b) and np.array_equal(a, c)
+
+
+def test_ns_transpose_equivariance():
+    # the bf16 operand is the same matrix either way; only the order of the
+    # norm's partial sums differs, so agreement is to bf16 noise, not bitwise
+    X = np.random.default_rng(5).standard_normal((160, 288))
+    a = _ns([X])[0][0]
+    b = _ns([np.ascontiguousarray(X.T)])[0][0]
+    assert rel_fro(b.T, a) < 5e-3
+
+
+def test_ns_output_band():
+    X = np.random.default_rng(0).standard_normal((256, 512))
+    got = _ns([X])[0][0]
+    sv = np.linalg.svd(got, compute_uv=False)
+    assert sv.max() < 1.2024 * 1.03 and sv.min() > 0.6799 * 0.97
+
+
+def test_mn_descriptor_reading():
+    """The apply phase reads X through an MN-major descriptor; only one of
+    the two stride readings reproduces the oracle (the default one)."""
+    X = np.random.default_rng(6).standard_normal((256, 512))
+    want = om.newton_schulz(X.astype(np.float32).astype(np.float64))
+    good = rel_fro(_ns([X])[0][0], want)
+    try:
+        B.mo_debug_set_mn_strides(1024, 8192)
+        other = rel_fro(_ns([X])[0][0], want)
+    finally:
+        B.mo_debug_set_mn_strides(8192, 1024)
+    assert good < NS_BF16_TOL
+    assert not other < NS_BF16_TOL

@@ -1,0 +1,111 @@
+"""GPU parity: sign_pack and sign_vote_update (bit-exact) and the AdamW tail,
+through the C ABI, against the oracle on seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import matrix_optimizers_gb300 as mo
+from oracle import adamw as oa
+from oracle import bf16 as ob
+from oracle import sign as osg
+from tests.gpu_helpers import dev, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _words_np(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def _signed_input(shape, seed):
+    rng = np.random.default_rng(seed)
+    U = rng.standard_normal(shape).astype(np.float32)
+    flat = U.reshape(-1)
+    flat[::7] = 0.0
+    flat[3::11] = -0.0
+    flat[5::13] = np.nan
+    flat[1::17] = -1e-30
+    return U
+
+
+@pytest.mark.parametrize("shape,ld", [((1, 1), None), ((3, 7), 8), ((5, 33), 40), ((64, 64), None),
+                                      ((100, 257), 264), ((1, 4097), None), ((513, 1), 8),
+                                      ((2048, 2048), None)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sign_pack_bit_exact(shape, ld, dtype):
+    U = _signed_input(shape, sum(shape))
+    Ut = to_dev(U, dtype, ld)
+    nw = (U.size + 31) // 32
+    words = torch.full((nw + 4,), -1, dtype=torch.int32, device=dev())    # canary after the end
+    mo.sign_pack(Ut, words[:nw])
+    torch.cuda.synchronize()
+    stored = to_np(Ut)        # the values the kernel saw (bf16-rounded for bf16)
+    want = osg.pack_bits(stored)
+    got = _words_np(words)
+    assert np.array_equal(got[:nw], want)
+    assert np.all(got[nw:] == 0xFFFFFFFF)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 13, 64, 128])
+@pytest.mark.parametrize("shape,ld", [((1, 5), 8), ((33, 95), 96), ((64, 64), None), ((2048, 2048), None)])
+@pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
+def test_vote_update_bit_exact(M, shape, ld, wdtype):
+    if M > 13 and shape[0] * shape[1] > 100_000:
+        pytest.skip("large voter counts are covered on the smaller shapes")
+    rng = np.random.default_rng(M * 1000 + shape[0])
+    numel = shape[0] * shape[1]
+    nw = (numel + 31) // 32
+    bufs = [rng.integers(0, 2 ** 32, size=nw, dtype=np.uint64).astype(np.uint32) for _ in range(M)]
+    # tail bits beyond numel are zero in a packed buffer
+    if numel % 32:
+        for b in bufs:
+            b[-1] &= np.uint32((1 << (numel % 32)) - 1)
+    words = [torch.from_numpy(b.view(np.int32).copy()).to(dev()) for b in bufs]
+    W = (0.02 * rng.standard_normal(shape)).astype(np.float32)
+    Wt = to_dev(W, wdtype, ld)
+    W_stored = to_np(Wt)
+    lr = 1e-3
+    mo.sign_vote_update(words, Wt, lr)
+    torch.cuda.synchronize()
+    want = osg.vote_update(W_stored, bufs, lr, "bf16" if wdtype == torch.bfloat16 else "f32")
+    got = to_np(Wt)
+    assert np.array_equal(got, want)
+    if ld is not None:   # padding columns (NaN-filled) are left untouched
+        full = Wt.as_strided((shape[0], ld), (ld, 1))
+        assert torch.isnan(full[:, shape[1]:].float()).all()
+
+
+def test_vote_ties_go_plus():
+    # M = 2 with opposite signs everywhere: every vote is a tie -> +1
+    numel = 64 * 64
+    a = np.full((numel + 31) // 32, 0xFFFFFFFF, dtype=np.uint32)
+    b = np.zeros_like(a)
+    words = [torch.from_numpy(x.view(np.int32).copy()).to(dev()) for x in (a, b)]
+    W = torch.zeros(64, 64, device=dev())
+    mo.sign_vote_update(words, W, 0.5)
+    torch.cuda.synchronize()
+    assert torch.all(W == -0.5)
+
+
+@pytest.mark.parametrize("numel", [1, 3, 1001, 36_864, 4_000_003])
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_adamw_tail_matches_oracle(numel, wd):
+    rng = np.random.default_rng(numel)
+    W = (0.02 * rng.standard_normal(numel)).astype(np.float32)
+    m = np.zeros(numel)
+    v = np.zeros(numel)
+    tW, tm_, tv = (torch.from_numpy(x.astype(np.float32)).to(dev()) for x in (W, m, v))
+    Wr, mr, vr = W.astype(np.float64), m, v
+    for t in range(1, 4):
+        g = (1e-3 * rng.standard_normal(numel)).astype(np.float32)
+        tg = torch.from_numpy(g).to(dev())
+        tail = mo.make_tail(tW, tg, tm_, tv, step=t, lr=1e-3, weight_decay=wd)
+        cfg = mo.make_cfg()
+        mo.muon_step_batched([], cfg, None, tail=tail)
+        Wr, mr, vr = oa.adamw_step(Wr, g, mr, vr, t, lr=1e-3, weight_decay=wd)
+    torch.cuda.synchronize()
+    gotW = tW.cpu().numpy().astype(np.float64)
+    # float32 state: |dW| error ~ float32 rounding of W plus ~1e-6 relative of each update
+    assert np.max(np.abs(gotW - Wr)) <= 1e-5 * 1e-3 * 3 + 4 * np.max(np.abs(Wr)) * 2 ** -23
+    np.testing.assert_allclose(tm_.cpu().numpy(), mr, rtol=1e-5, atol=1e-12)
+    np.testing.assert_allclose(tv.cpu().numpy(), vr, rtol=1e-5, atol=1e-16)

@@ -78,13 +78,24 @@ def _normal(key, shape, std):
 
 
 def matrix_inputs(shapes, index, seed_w=0, seed_g=1, w_std=0.02, g_std=1e-3):
-    """Inputs of matrix ``index`` of a set: dict of float32 W, G, M0 (zeros)."""
+    """Inputs of matrix ``index`` of a set: dict of float32 W and G; the
+    momentum starts at zero (no array is stored for it)."""
     r, c = shapes[index]
     return {
         "W": _normal([seed_w, index], (r, c), w_std),
         "G": _normal([seed_g, index], (r, c), g_std),
-        "M0": np.zeros((r, c), dtype=np.float32),
     }
+
+
+def matrix_set_inputs(shapes, indices=None, threads=None, **kw):
+    """matrix_inputs for many matrices, drawn in parallel threads (each matrix
+    has its own generator, so the result does not depend on the threading)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+    idx = list(range(len(shapes))) if indices is None else list(indices)
+    threads = threads or min(16, len(os.sched_getaffinity(0)))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda i: matrix_inputs(shapes, i, **kw), idx))
 
 
 def single_matrix_inputs(rows=256, cols=512, seed=0):
