@@ -366,19 +366,21 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             for (int ch = 0; ch < 4; ++ch) {
                 const int col = half * 128 + ch * 32;
                 uint32_t r[32];
+                __syncwarp();
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(acc * kTcBN + col),
                                    r);
                 tmem_wait_ld();
-                if (!row_ok) continue;
-                float v[32];
+                if (row_ok) {
+                    float v[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-                const int j0 = td.tj * kTcBN + col;
-                if (p.phase == kApply)
-                    epi_apply(p, md, i, j0, v);
-                else
-                    epi_symmetric(p, md, i, j0, v);
+                    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+                    const int j0 = td.tj * kTcBN + col;
+                    if (p.phase == kApply)
+                        epi_apply(p, md, i, j0, v);
+                    else
+                        epi_symmetric(p, md, i, j0, v);
+                }
             }
             tc_fence_before();
             __syncwarp();
