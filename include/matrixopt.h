@@ -141,7 +141,8 @@ int ns_orthogonalize(const void* const* X, void* const* out,
  * cols, leading dimension ld, dtype MO_F32/MO_BF16) goes to bit (j % 32) of
  * words[j / 32]; the bit is 1 unless U_j < 0 (so +0, -0 and NaN give 1, the
  * sign(0) = +1 rule).  words has ceil(rows*cols/32) uint32 entries; unused
- * bits of the last word are written 0.  No workspace. */
+ * bits of the last word are written 0.  No workspace.  Only element alignment
+ * is required of U (4 or 2 bytes) and of words (4 bytes), and any ld >= cols. */
 int sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
               uint32_t* words, mo_stream_t stream);
 
@@ -151,7 +152,8 @@ int sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
  * element, with c of the M workers voting +1, vote = +1 if 2c >= M (ties go
  * to +1) else -1, and W <- W - lr*vote in float32 (one rounding; a bf16 W is
  * rounded to bf16 once).  1 <= M <= 128 (MO_ERR_INVALID_ARG for M <= 0,
- * MO_ERR_UNSUPPORTED above 128). */
+ * MO_ERR_UNSUPPORTED above 128).  W needs element alignment only, any
+ * ld >= cols; word buffers need 4-byte alignment. */
 int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols,
                      void* W, int w_dtype, int64_t ld, float lr, mo_stream_t stream);
 

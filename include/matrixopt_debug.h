@@ -46,6 +46,26 @@ int mo_debug_sm_count(void);
  * affects launches issued after the call. */
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
+/* Launch tracing, for measurement.  mo_trace_enable(capacity) makes every
+ * later kernel launch of the calling thread (any entry point) record a CUDA
+ * event before and after it on the call's stream, for up to `capacity`
+ * launches (events are created once and reused; no device memory).
+ * capacity 0 disables tracing.  mo_trace_read() synchronises on the last
+ * recorded event, writes up to `cap` entries (kind, milliseconds) of the
+ * launches recorded since the previous read, sets *count, and starts a new
+ * record.  Kinds: */
+#define MO_K_MOMENTUM 1   /* fused momentum + norm partials (+ NS operand) */
+#define MO_K_FINALIZE 2   /* per-matrix norm finalisation */
+#define MO_K_GRAM     3   /* NS A = X X^T   (tensor cores, or CUDA cores in fp32 mode) */
+#define MO_K_POLY     4   /* NS B = bA + cA^2 */
+#define MO_K_APPLY    5   /* NS X = aX + BX (+ fused update on the last step) */
+#define MO_K_NS0      6   /* zero-step normalise/update */
+#define MO_K_ADAMW    7
+#define MO_K_PACK     8
+#define MO_K_VOTE     9
+int mo_trace_enable(int capacity);
+int mo_trace_read(int32_t* kinds, float* ms, int cap, int* count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,7 +84,13 @@ _SIGNATURES = [
                                    c_int32, ctypes.POINTER(mo_ns_view)]),
     ("mo_debug_sm_count", c_int32, []),
     ("mo_debug_set_mn_strides", c_int32, [ctypes.c_uint32, ctypes.c_uint32]),
+    ("mo_trace_enable", c_int32, [c_int32]),
+    ("mo_trace_read", c_int32, [ctypes.POINTER(c_int32), ctypes.POINTER(c_float), c_int32,
+                                ctypes.POINTER(c_int32)]),
 ]
+
+TRACE_KINDS = {1: "momentum_norm", 2: "norm_finalize", 3: "ns_gram", 4: "ns_poly", 5: "ns_apply",
+               6: "ns_k0", 7: "adamw", 8: "sign_pack", 9: "vote_update"}
 
 _lib = None
 _lock = threading.Lock()
@@ -268,3 +274,18 @@ def mo_debug_ns_view(shapes, index, precision=MO_NS_BF16):
 
 def mo_debug_set_mn_strides(lbo, sbo):
     _check(load().mo_debug_set_mn_strides(lbo, sbo))
+
+
+def mo_trace_enable(capacity):
+    """Record a CUDA event pair around each of the next ``capacity`` launches
+    issued from this thread (0 disables)."""
+    _check(load().mo_trace_enable(capacity))
+
+
+def mo_trace_read(cap=1 << 16):
+    """[(kind name, milliseconds), ...] of the launches traced since the last read."""
+    kinds = (c_int32 * cap)()
+    ms = (c_float * cap)()
+    count = c_int32(0)
+    _check(load().mo_trace_read(kinds, ms, cap, ctypes.byref(count)))
+    return [(TRACE_KINDS.get(kinds[i], str(kinds[i])), ms[i]) for i in range(min(cap, count.value))]

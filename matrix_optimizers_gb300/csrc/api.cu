@@ -259,6 +259,31 @@ struct NsOpts {
     float mu, a, b, c, alpha, decay;
 };
 
+// ------------------------------------------------------------ launch trace
+// Optional per-thread record of a CUDA event pair around each kernel launch
+// (enabled by mo_trace_enable), read back by mo_trace_read.
+struct Trace {
+    int capacity = 0;
+    int count = 0;
+    std::vector<cudaEvent_t> begin, end;
+    std::vector<int32_t> kind;
+};
+thread_local Trace t_trace;
+
+template <typename F>
+cudaError_t traced(int kind, cudaStream_t s, F&& launch) {
+    Trace& t = t_trace;
+    const bool on = t.capacity > 0 && t.count < t.capacity;
+    if (on && cudaEventRecord(t.begin[t.count], s) != cudaSuccess) return cudaErrorUnknown;
+    cudaError_t e = launch();
+    if (on && e == cudaSuccess) {
+        if (cudaEventRecord(t.end[t.count], s) != cudaSuccess) return cudaErrorUnknown;
+        t.kind[t.count] = kind;
+        ++t.count;
+    }
+    return e;
+}
+
 thread_local std::vector<uint8_t> t_stage;
 
 // Builds the control block for `jobs`, uploads it into `ws` and launches the
@@ -382,11 +407,14 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     mp.fp32_operand = o.precision == MO_NS_FP32;
     mp.partials = reinterpret_cast<float*>(base + L.partials);
     const int mom_grid = static_cast<int>(std::min<int64_t>(L.mom_tiles, static_cast<int64_t>(nsm) * 8));
-    if ((e = launch_momentum_norm(mp, mom_grid, stream)) != cudaSuccess) return MO_ERR_CUDA;
-    if ((e = launch_norm_finalize(dmats, mp.nmats, mp.partials, stream)) != cudaSuccess) return MO_ERR_CUDA;
+    e = traced(MO_K_MOMENTUM, stream, [&] { return launch_momentum_norm(mp, mom_grid, stream); });
+    if (e != cudaSuccess) return MO_ERR_CUDA;
+    e = traced(MO_K_FINALIZE, stream, [&] { return launch_norm_finalize(dmats, mp.nmats, mp.partials, stream); });
+    if (e != cudaSuccess) return MO_ERR_CUDA;
 
     if (o.steps == 0) {
-        e = launch_ns_k0(mp, o.alpha, o.decay, o.apply_update, mom_grid, stream);
+        e = traced(MO_K_NS0, stream,
+                   [&] { return launch_ns_k0(mp, o.alpha, o.decay, o.apply_update, mom_grid, stream); });
         return map_cuda(e);
     }
     NsLaunch np;
@@ -409,8 +437,10 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
             np.cta_range = reinterpret_cast<const int2*>(base + L.ranges[ph]);
             np.ntiles = static_cast<int32_t>(L.ntiles[ph]);
             np.idesc = idesc_bf16_f32(kTcBM, kTcBN, ph == kApply ? 1u : 0u);
-            e = o.precision == MO_NS_BF16 ? launch_ns_tc_phase(np, grids[ph], stream)
-                                          : launch_ns_fp32_phase(np, grids[ph], stream);
+            e = traced(MO_K_GRAM + ph, stream, [&] {
+                return o.precision == MO_NS_BF16 ? launch_ns_tc_phase(np, grids[ph], stream)
+                                                 : launch_ns_fp32_phase(np, grids[ph], stream);
+            });
             if (e != cudaSuccess) return MO_ERR_CUDA;
         }
     }
@@ -513,7 +543,7 @@ int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, cons
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (tail != nullptr && tail->numel > 0) {
-        if (launch_adamw(*tail, s) != cudaSuccess) return MO_ERR_CUDA;
+        if (traced(MO_K_ADAMW, s, [&] { return launch_adamw(*tail, s); }) != cudaSuccess) return MO_ERR_CUDA;
     }
     NsOpts o;
     o.precision = cfg->ns_precision;
@@ -587,10 +617,11 @@ int sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, 
     if (!valid_dtype(dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return MO_OK;
     if (ld < cols || U == nullptr || words == nullptr) return MO_ERR_INVALID_ARG;
-    if (!aligned16(U) || (static_cast<size_t>(ld) * elem_size(dtype)) % 16 != 0 ||
-        (reinterpret_cast<uintptr_t>(words) & 3u) != 0)
+    // element accesses only: element alignment suffices
+    if ((reinterpret_cast<uintptr_t>(U) % elem_size(dtype)) != 0 || (reinterpret_cast<uintptr_t>(words) & 3u) != 0)
         return MO_ERR_ALIGNMENT;
-    return map_cuda(launch_sign_pack(U, dtype, rows, cols, ld, words, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return map_cuda(traced(MO_K_PACK, s, [&] { return launch_sign_pack(U, dtype, rows, cols, ld, words, s); }));
 }
 
 int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols, void* W, int w_dtype,
@@ -603,9 +634,11 @@ int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t 
         if (words[m] == nullptr) return MO_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(words[m]) & 3u) != 0) return MO_ERR_ALIGNMENT;
     }
-    if (!aligned16(W) || (static_cast<size_t>(ld) * elem_size(w_dtype)) % 16 != 0) return MO_ERR_ALIGNMENT;
-    return map_cuda(launch_sign_vote_update(words, M, rows, cols, W, w_dtype, ld, lr,
-                                            reinterpret_cast<cudaStream_t>(stream)));
+    if ((reinterpret_cast<uintptr_t>(W) % elem_size(w_dtype)) != 0) return MO_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return map_cuda(traced(MO_K_VOTE, s, [&] {
+        return launch_sign_vote_update(words, M, rows, cols, W, w_dtype, ld, lr, s);
+    }));
 }
 
 int plan_owners(const int64_t* rows, const int64_t* cols, int n, int world, int ns_steps, double w_bytes,
@@ -702,6 +735,36 @@ int mo_debug_sm_count(void) {
     int c = 0;
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return c;
+}
+
+int mo_trace_enable(int capacity) {
+    Trace& t = t_trace;
+    if (capacity < 0) return MO_ERR_INVALID_ARG;
+    for (int i = static_cast<int>(t.begin.size()); i < capacity; ++i) {
+        cudaEvent_t b, e;
+        if (cudaEventCreate(&b) != cudaSuccess) return MO_ERR_CUDA;
+        if (cudaEventCreate(&e) != cudaSuccess) return MO_ERR_CUDA;
+        t.begin.push_back(b);
+        t.end.push_back(e);
+        t.kind.push_back(0);
+    }
+    t.capacity = capacity;
+    t.count = 0;
+    return MO_OK;
+}
+
+int mo_trace_read(int32_t* kinds, float* ms, int cap, int* count) {
+    Trace& t = t_trace;
+    if (count == nullptr || cap < 0 || (cap > 0 && (kinds == nullptr || ms == nullptr))) return MO_ERR_INVALID_ARG;
+    const int n = std::min(cap, t.count);
+    if (t.count > 0 && cudaEventSynchronize(t.end[t.count - 1]) != cudaSuccess) return MO_ERR_CUDA;
+    for (int i = 0; i < n; ++i) {
+        kinds[i] = t.kind[i];
+        if (cudaEventElapsedTime(&ms[i], t.begin[i], t.end[i]) != cudaSuccess) return MO_ERR_CUDA;
+    }
+    *count = t.count;
+    t.count = 0;
+    return MO_OK;
 }
 
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo) {

@@ -135,7 +135,9 @@ def test_sign_call_validation_without_device(lib):
     assert lib.sign_pack(None, 0, 4, 4, 4, None, None) == B.MO_ERR_INVALID_ARG
     assert lib.sign_pack(ctypes.c_void_p(256), 5, 4, 4, 4, ctypes.c_void_p(256), None) == B.MO_ERR_INVALID_ARG
     assert lib.sign_pack(ctypes.c_void_p(258), 0, 4, 4, 4, ctypes.c_void_p(256), None) == B.MO_ERR_ALIGNMENT
-    assert lib.sign_pack(ctypes.c_void_p(256), 1, 4, 4, 4, ctypes.c_void_p(256), None) == B.MO_ERR_ALIGNMENT
+    assert lib.sign_pack(ctypes.c_void_p(257), 1, 4, 4, 4, ctypes.c_void_p(256), None) == B.MO_ERR_ALIGNMENT
+    assert lib.sign_pack(ctypes.c_void_p(256), 0, 4, 4, 4, ctypes.c_void_p(258), None) == B.MO_ERR_ALIGNMENT
+    assert lib.sign_pack(ctypes.c_void_p(256), 0, 4, 4, 3, ctypes.c_void_p(256), None) == B.MO_ERR_INVALID_ARG
     assert lib.sign_pack(ctypes.c_void_p(256), 0, 0, 4, 4, ctypes.c_void_p(256), None) == B.MO_OK
     words = (ctypes.c_void_p * 2)(256, 512)
     assert lib.sign_vote_update(words, 0, 4, 4, ctypes.c_void_p(256), 0, 4, 1e-3, None) == B.MO_ERR_INVALID_ARG
@@ -143,7 +145,9 @@ def test_sign_call_validation_without_device(lib):
         B.MO_ERR_UNSUPPORTED
     bad = (ctypes.c_void_p * 2)(256, 0)
     assert lib.sign_vote_update(bad, 2, 4, 4, ctypes.c_void_p(256), 0, 4, 1e-3, None) == B.MO_ERR_INVALID_ARG
-    assert lib.sign_vote_update(words, 2, 4, 4, ctypes.c_void_p(260), 0, 4, 1e-3, None) == B.MO_ERR_ALIGNMENT
+    assert lib.sign_vote_update(words, 2, 4, 4, ctypes.c_void_p(258), 0, 4, 1e-3, None) == B.MO_ERR_ALIGNMENT
+    odd = (ctypes.c_void_p * 2)(256, 514)
+    assert lib.sign_vote_update(odd, 2, 4, 4, ctypes.c_void_p(256), 0, 4, 1e-3, None) == B.MO_ERR_ALIGNMENT
 
 
 def test_debug_view_offsets_are_disjoint():

@@ -90,8 +90,10 @@ def test_weight_decay_and_update_scale():
 
 
 def test_bf16_state_dtypes():
+    # W starts at 0 so that bf16 storage keeps the update at bf16 relative
+    # precision (a unit-scale W would have a bf16 spacing above the update)
     rng = np.random.default_rng(10)
-    inp = {"W": rng.standard_normal((192, 256)).astype(np.float32),
+    inp = {"W": np.zeros((192, 256), dtype=np.float32),
            "G": rng.standard_normal((192, 256)).astype(np.float32),
            "M0": rng.standard_normal((192, 256)).astype(np.float32)}
     W = to_dev(inp["W"], torch.bfloat16)

@@ -19,7 +19,9 @@ A, Bc, C = om.NS_A, om.NS_B, om.NS_C
 def _ns(X_list, steps=5, precision=mo.MO_NS_BF16, out_dtype=torch.float32, coeffs=(A, Bc, C), lds=None):
     shapes = [tuple(x.shape) for x in X_list]
     ws = workspace(mo.ns_workspace_bytes(shapes, precision))
-    lds = lds or [None] * len(X_list)
+    # the ABI wants ld * element size a multiple of 16 bytes: pad odd widths
+    # (the padding is NaN-filled, so a kernel reading it would show)
+    lds = lds or [None if s[1] % 8 == 0 else (s[1] + 7) // 8 * 8 for s in shapes]
     Xt = [to_dev(x, torch.float32, ld) for x, ld in zip(X_list, lds)]
     outs = []
     for x, ld in zip(X_list, lds):

@@ -6,7 +6,6 @@ import torch
 
 import matrix_optimizers_gb300 as mo
 from oracle import adamw as oa
-from oracle import bf16 as ob
 from oracle import sign as osg
 from tests.gpu_helpers import dev, to_dev, to_np
 
@@ -107,5 +106,8 @@ def test_adamw_tail_matches_oracle(numel, wd):
     gotW = tW.cpu().numpy().astype(np.float64)
     # float32 state: |dW| error ~ float32 rounding of W plus ~1e-6 relative of each update
     assert np.max(np.abs(gotW - Wr)) <= 1e-5 * 1e-3 * 3 + 4 * np.max(np.abs(Wr)) * 2 ** -23
-    np.testing.assert_allclose(tm_.cpu().numpy(), mr, rtol=1e-5, atol=1e-12)
-    np.testing.assert_allclose(tv.cpu().numpy(), vr, rtol=1e-5, atol=1e-16)
+    # m is a signed running sum: elements near zero carry the float32 rounding of
+    # terms of size ~|g|, so the bound is relative to the terms, not to m itself
+    gm, gv = tm_.cpu().numpy().astype(np.float64), tv.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(gm - mr)) <= 16 * 2 ** -24 * np.max(np.abs(mr))
+    assert np.max(np.abs(gv - vr) / vr.clip(min=1e-300)) <= 16 * 2 ** -24
