@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <memory>
 #include <mutex>
 #include <queue>
 #include <vector>
@@ -284,24 +285,55 @@ cudaError_t traced(int kind, cudaStream_t s, F&& launch) {
     return e;
 }
 
-thread_local std::vector<uint8_t> t_stage;
+// A built control block (descriptor table, tensor maps, scheduled tile
+// lists) for one request placed in one workspace.  The staged bytes are
+// uploaded on every call; building them (tensor-map encoding, LPT
+// scheduling) is cached by everything that shapes their content.
+struct Plan {
+    std::vector<int64_t> key;
+    Layout L;
+    std::vector<uint8_t> stage;
+    int grids[3] = {0, 0, 0};
+};
 
-// Builds the control block for `jobs`, uploads it into `ws` and launches the
-// whole path on `stream`.
-int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+std::mutex g_plan_mu;
+std::vector<std::shared_ptr<const Plan>> g_plans;   // most recently used first
+constexpr size_t kPlanCacheSize = 16;
+
+std::vector<int64_t> plan_key(const std::vector<Job>& jobs, int precision, const void* ws) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+    std::vector<int64_t> k;
+    k.reserve(4 + jobs.size() * 12);
+    k.push_back(dev);
+    k.push_back(precision);
+    k.push_back(static_cast<int64_t>(reinterpret_cast<uintptr_t>(ws)));
+    k.push_back(device_sm_count());
+    for (const Job& j : jobs) {
+        const int64_t f[12] = {j.rows, j.cols, j.ld, j.src_dtype, j.g_dtype, j.w_dtype, j.out_dtype, j.has_momentum,
+                               static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.src)),
+                               static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.grad)),
+                               static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.W)),
+                               static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.out))};
+        k.insert(k.end(), f, f + 12);
+    }
+    return k;
+}
+
+int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::shared_ptr<Plan>& out) {
     std::vector<std::pair<int64_t, int64_t>> dims;
     dims.reserve(jobs.size());
     for (const Job& j : jobs) dims.push_back({j.rows, j.cols});
-    if (jobs.empty()) return MO_OK;
-    const Layout L = make_layout(dims, o.precision);
-    int st = validate_ws(ws, ws_bytes, L.total);
-    if (st != MO_OK) return st;
-    if (o.precision == MO_NS_BF16 && !get_encode()) return MO_ERR_CUDA;
+    auto plan = std::make_shared<Plan>();
+    plan->L = make_layout(dims, precision);
+    const Layout& L = plan->L;
+    if (precision == MO_NS_BF16 && !get_encode()) return MO_ERR_CUDA;
 
     uint8_t* base = static_cast<uint8_t*>(ws);
     const int nsm = device_sm_count();
-    t_stage.assign(L.ctl_bytes, 0);
-    uint8_t* h = t_stage.data();
+    plan->stage.assign(L.ctl_bytes, 0);
+    uint8_t* h = plan->stage.data();
+    const NsOpts o{precision, 0, 0, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     MatDesc* hm = reinterpret_cast<MatDesc*>(h + L.mats);
     CUtensorMap* htm = reinterpret_cast<CUtensorMap*>(h + L.tmaps);
     const CUtensorMap* dtm = reinterpret_cast<const CUtensorMap*>(base + L.tmaps);
@@ -354,7 +386,7 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     }
 
     // tile lists per phase
-    int grids[3] = {0, 0, 0};
+    int* grids = plan->grids;
     for (int ph = 0; ph < 3; ++ph) {
         std::vector<TileDesc> tiles;
         tiles.reserve(static_cast<size_t>(L.ntiles[ph]));
@@ -394,8 +426,48 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
             grids[ph] = static_cast<int>(tiles.size());
         }
     }
+    out = plan;
+    return MO_OK;
+}
 
-    cudaError_t e = cudaMemcpyAsync(base, h, L.ctl_bytes, cudaMemcpyHostToDevice, stream);
+int get_plan(const std::vector<Job>& jobs, int precision, void* ws, std::shared_ptr<const Plan>& out) {
+    std::vector<int64_t> key = plan_key(jobs, precision, ws);
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        for (size_t i = 0; i < g_plans.size(); ++i) {
+            if (g_plans[i]->key == key) {
+                out = g_plans[i];
+                std::rotate(g_plans.begin(), g_plans.begin() + i, g_plans.begin() + i + 1);
+                return MO_OK;
+            }
+        }
+    }
+    std::shared_ptr<Plan> p;
+    int st = build_plan(jobs, precision, ws, p);
+    if (st != MO_OK) return st;
+    p->key = std::move(key);
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    g_plans.insert(g_plans.begin(), p);
+    if (g_plans.size() > kPlanCacheSize) g_plans.pop_back();
+    out = p;
+    return MO_OK;
+}
+
+// Uploads the (cached) control block for `jobs` into `ws` and launches the
+// whole path on `stream`.
+int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+    if (jobs.empty()) return MO_OK;
+    int st = validate_ws(ws, ws_bytes, 0);
+    if (st != MO_OK) return st;
+    std::shared_ptr<const Plan> plan;
+    if ((st = get_plan(jobs, o.precision, ws, plan)) != MO_OK) return st;
+    const Layout& L = plan->L;
+    if ((st = validate_ws(ws, ws_bytes, L.total)) != MO_OK) return st;
+    const int* grids = plan->grids;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    const int nsm = device_sm_count();
+
+    cudaError_t e = cudaMemcpyAsync(base, plan->stage.data(), L.ctl_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return MO_ERR_CUDA;
 
     const MatDesc* dmats = reinterpret_cast<const MatDesc*>(base + L.mats);

@@ -22,6 +22,8 @@
 // abort flag, records an error code and unwinds after draining copies.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -401,8 +403,16 @@ int tc_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_ns_tc_phase(const NsLaunch& p, int grid, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    static std::atomic<uint64_t> attr_set{0};   // one bit per device ordinal
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    const uint64_t bit = uint64_t(1) << (dev & 63);
+    if (!(attr_set.load() & bit)) {
+        e = cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set.fetch_or(bit);
+    }
     ns_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
     return cudaGetLastError();
 }
