@@ -136,6 +136,32 @@ int ns_orthogonalize(const void* const* X, void* const* out,
                      float a, float b, float c, int precision,
                      void* ws, size_t ws_bytes, mo_stream_t stream);
 
+/* ns_orthogonalize for ONE matrix (bf16 tensor-core mode) that allocates
+ * nothing and takes no workspace.  The pages have no counterpart: this entry
+ * point exists for callers that cannot allocate device memory, such as a
+ * plugin handed only its input and output buffers by a host framework that
+ * owns and accounts for every byte of device memory, or a latency-critical
+ * loop where a cudaMalloc would synchronise the device.
+ *   - Scratch: a fixed array of MO_NOALLOC_SCRATCH_BYTES (32 MiB) compiled
+ *     into the library in device global memory; every GPU that loads the
+ *     library holds it until the process exits.
+ *   - Size limit: ns_workspace_bytes() for this shape must not exceed
+ *     MO_NOALLOC_SCRATCH_BYTES, else MO_ERR_UNSUPPORTED (for example
+ *     768 x 3072 and 1024 x 2048 fit, 2048 x 2048 does not).
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array per device and it keeps the last
+ *     call's contents; calls whose work overlaps on the GPU (other streams,
+ *     other threads) race and corrupt each other's results.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.  The
+ *     device error word is not exposed for this entry point.
+ * Arguments as ns_orthogonalize with n = 1 (X, out device pointers). */
+#define MO_NOALLOC_SCRATCH_BYTES (32u << 20)
+int ns_orthogonalize_noalloc(const void* X, void* out, int64_t rows, int64_t cols, int64_t ld,
+                             int in_dtype, int out_dtype, int steps, float a, float b, float c,
+                             mo_stream_t stream);
+
 /* Sign extraction and 1-bit packing (SignMuon §2 step 2 and the all-gather
  * variant of step 3).  Element j of the row-major flattening of U (rows x
  * cols, leading dimension ld, dtype MO_F32/MO_BF16) goes to bit (j % 32) of

@@ -71,6 +71,8 @@ _SIGNATURES = [
                                    ctypes.POINTER(c_int64), ctypes.POINTER(c_int64),
                                    ctypes.POINTER(c_int64), c_int32, c_int32, c_int32, c_int32,
                                    c_float, c_float, c_float, c_int32, c_void_p, c_size_t, c_void_p]),
+    ("ns_orthogonalize_noalloc", c_int32, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int32, c_int32,
+                                           c_int32, c_float, c_float, c_float, c_void_p]),
     ("sign_pack", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     ("sign_vote_update", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
                                    c_int32, c_int64, c_float, c_void_p]),
@@ -230,6 +232,17 @@ def ns_orthogonalize(X, out, steps, ws, a=3.4445, b=-4.7750, c=2.0315, precision
     _check(load().ns_orthogonalize(xs, os_, rows, cols, ld, n, in_dt, out_dt, steps, a, b, c,
                                    precision, _ptr(ws), ws.numel() if ws is not None else 0,
                                    _stream(stream)))
+
+
+def ns_orthogonalize_noalloc(X, out, steps, a=3.4445, b=-4.7750, c=2.0315, stream=None):
+    """out = NS_steps(X/||X||_F) for one matrix, using the library's fixed
+    device scratch instead of a workspace (for callers that cannot allocate
+    device memory; see include/matrixopt.h for the size limit)."""
+    if _ld(X) != _ld(out):
+        raise MoError(MO_ERR_INVALID_ARG, "X and out must share the leading dimension")
+    _check(load().ns_orthogonalize_noalloc(_ptr(X), _ptr(out), X.size(0), X.size(1), _ld(X),
+                                           dtype_code(X.dtype), dtype_code(out.dtype), steps, a, b, c,
+                                           _stream(stream)))
 
 
 def sign_pack(U, words, stream=None):
