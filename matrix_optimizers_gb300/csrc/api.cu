@@ -396,12 +396,21 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
                 const int nkb = static_cast<int>(ceil_div(ph == kGram ? s.n : s.m, kTcBK));
                 const int64_t tr = ceil_div(s.m, kTcBM);
                 const int64_t tc = ceil_div(ph == kApply ? s.n : s.m, kTcBN);
-                for (int64_t I = 0; I < tr; ++I)
-                    for (int64_t J = 0; J < tc; ++J) {
-                        if (ph != kApply && std::min(J * kTcBN + kTcBN - 1, s.m - 1) < I * kTcBM) continue;
-                        tiles.push_back(TileDesc{static_cast<int32_t>(i), static_cast<int32_t>(I),
-                                                 static_cast<int32_t>(J), nkb});
-                    }
+                if (ph == kApply) {
+                    // column-block-major: the CTAs of one wave share a few
+                    // 256-column panels of X while B (m x m) stays in L2
+                    for (int64_t J = 0; J < tc; ++J)
+                        for (int64_t I = 0; I < tr; ++I)
+                            tiles.push_back(TileDesc{static_cast<int32_t>(i), static_cast<int32_t>(I),
+                                                     static_cast<int32_t>(J), nkb});
+                } else {
+                    for (int64_t I = 0; I < tr; ++I)
+                        for (int64_t J = 0; J < tc; ++J) {
+                            if (std::min(J * kTcBN + kTcBN - 1, s.m - 1) < I * kTcBM) continue;
+                            tiles.push_back(TileDesc{static_cast<int32_t>(i), static_cast<int32_t>(I),
+                                                     static_cast<int32_t>(J), nkb});
+                        }
+                }
             } else {
                 const int nkb = static_cast<int>(ceil_div(ph == kGram ? s.n : s.m, kFpBK));
                 const int64_t tr = ceil_div(s.m, kFpBM);

@@ -267,10 +267,85 @@ __global__ void __launch_bounds__(256) sign_pack_kernel(const T* __restrict__ U,
     }
 }
 
+// Fast path when every run of 8 elements lies in one row and starts 16-byte
+// aligned (cols % 8 == 0, ld % 8 == 0, U 16-byte aligned): lane l loads 8
+// consecutive elements with 16-byte loads, forms their 8 sign bits, and 4
+// neighbouring lanes OR their bytes into one word.  A warp packs 32 words
+// (1024 elements) per iteration.
+__device__ __forceinline__ uint32_t sign_byte(const float (&x)[8]) {
+    uint32_t b = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) b |= (x[k] < 0.f ? 0u : 1u) << k;
+    return b;
+}
+__device__ __forceinline__ void load8(const float* p, float (&x)[8]) {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void load8(const bf16* p, float (&x)[8]) {
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        x[2 * q] = __low2float(h[q]);
+        x[2 * q + 1] = __high2float(h[q]);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) sign_pack_vec_kernel(const T* __restrict__ U, int64_t rows, int64_t cols,
+                                                            int64_t ld, uint32_t* __restrict__ words,
+                                                            int64_t nwords) {
+    constexpr int kSub = 4;                       // 4 x 256 elements per warp iteration
+    const int lane = threadIdx.x & 31;
+    const int64_t noct = rows * cols / 8;         // runs of 8 elements
+    const int64_t opr = cols / 8;                 // runs per row
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t o0 = warp * 32 * kSub; o0 < noct; o0 += nwarps * 32 * kSub) {
+        int64_t o = o0 + lane;
+        int64_t r = o / opr, c8 = o - r * opr;
+        float x[kSub][8];
+#pragma unroll
+        for (int u = 0; u < kSub; ++u) {
+            if (o + 32 * u < noct) {
+                load8(U + r * ld + c8 * 8, x[u]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x[u][k] = -1.f;     // beyond the matrix: bit 0
+            }
+            c8 += 32;
+            while (c8 >= opr) { c8 -= opr; ++r; }
+        }
+#pragma unroll
+        for (int u = 0; u < kSub; ++u) {
+            uint32_t v = sign_byte(x[u]) << (8 * (lane & 3));
+            v |= __shfl_xor_sync(0xffffffffu, v, 1);
+            v |= __shfl_xor_sync(0xffffffffu, v, 2);
+            const int64_t w = (o0 + 32 * u) / 4 + (lane >> 2);
+            if ((lane & 3) == 0 && w < nwords) words[w] = v;
+        }
+    }
+}
+
 cudaError_t launch_sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
                              uint32_t* words, cudaStream_t s) {
     const int64_t nwords = (rows * cols + 31) / 32;
     if (nwords == 0) return cudaSuccess;
+    const bool vec = cols % 8 == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(U) & 15u) == 0;
+    if (vec) {
+        const int64_t warps_needed = (rows * cols / 8 + 127) / 128;
+        const int64_t blocks = (warps_needed + 7) / 8;
+        const int grid = static_cast<int>(blocks < device_sm_count() * 8LL ? blocks : device_sm_count() * 8LL);
+        if (dtype == MO_F32)
+            sign_pack_vec_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(U), rows, cols, ld, words,
+                                                             nwords);
+        else
+            sign_pack_vec_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(U), rows, cols, ld, words,
+                                                            nwords);
+        return cudaGetLastError();
+    }
     const int64_t warps_needed = (nwords + kPackWords - 1) / kPackWords;
     const int64_t blocks = (warps_needed + 7) / 8;
     const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
@@ -348,6 +423,98 @@ __global__ void __launch_bounds__(256) vote_update_kernel(const __grid_constant_
     }
 }
 
+// Bit-sliced count of +1 votes of 32 elements over the M buffers, compared
+// with ceil(M/2): bit k of the result is 1 when element k votes +1.
+__device__ __forceinline__ uint32_t vote_word(const VotePtrs& ptrs, int M, int nbits, uint32_t thr, int64_t w) {
+    uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int m = 0; m < M; ++m) {
+        uint32_t x = __ldcs(ptrs.w[m] + w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < nbits) {
+                const uint32_t carry = cnt[j] & x;
+                cnt[j] ^= x;
+                x = carry;
+            }
+        }
+    }
+    uint32_t gt = 0u, eq = 0xffffffffu;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+        if (j < nbits) {
+            if ((thr >> j) & 1u) {
+                eq &= cnt[j];
+            } else {
+                gt |= eq & cnt[j];
+                eq &= ~cnt[j];
+            }
+        }
+    }
+    return gt | eq;
+}
+
+template <typename T> struct Vec4;
+template <> struct Vec4<float> {
+    using type = float4;
+    static __device__ __forceinline__ void unpack(const float4& v, float (&x)[4]) { x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w; }
+    static __device__ __forceinline__ float4 pack(const float (&x)[4]) { return make_float4(x[0], x[1], x[2], x[3]); }
+};
+template <> struct Vec4<bf16> {
+    using type = uint2;
+    static __device__ __forceinline__ void unpack(const uint2& v, float (&x)[4]) {
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        x[0] = __low2float(h[0]); x[1] = __high2float(h[0]); x[2] = __low2float(h[1]); x[3] = __high2float(h[1]);
+    }
+    static __device__ __forceinline__ uint2 pack(const float (&x)[4]) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+        uint2 v;
+        v.x = *reinterpret_cast<uint32_t*>(&a);
+        v.y = *reinterpret_cast<uint32_t*>(&b);
+        return v;
+    }
+};
+
+// Fast path when runs of 4 elements lie in one row and are vector-aligned
+// (cols % 4 == 0, ld % 4 == 0, W aligned to 4 elements): a warp takes 32
+// words; lane l updates elements 128q + 4l .. +3 (q = 0..7) with 4-element
+// vector accesses, all loads issued before the stores.
+template <typename T>
+__global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_constant__ VotePtrs ptrs, int M, int nbits,
+                                                              uint32_t thr, int64_t rows, int64_t cols, int64_t ld,
+                                                              T* __restrict__ W, float lr, int64_t nwords) {
+    using V = typename Vec4<T>::type;
+    const int lane = threadIdx.x & 31;
+    const int64_t numel = rows * cols;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t base = warp * 32; base < nwords; base += nwarps * 32) {
+        const uint32_t plus = base + lane < nwords ? vote_word(ptrs, M, nbits, thr, base + lane) : 0u;
+        int64_t e = base * 32 + 4 * lane;
+        int64_t r = e / cols, c = e - r * cols;
+        int64_t idx[8];
+        V val[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            idx[q] = e + 128 * q < numel ? r * ld + c : -1;
+            if (idx[q] >= 0) val[q] = *reinterpret_cast<const V*>(W + idx[q]);
+            c += 128;
+            while (c >= cols) { c -= cols; ++r; }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t vw = __shfl_sync(0xffffffffu, plus, 4 * q + (lane >> 3));
+            const uint32_t bits = vw >> (4 * (lane & 7));
+            if (idx[q] >= 0) {
+                float x[4];
+                Vec4<T>::unpack(val[q], x);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[k] = ((bits >> k) & 1u) ? (x[k] - lr) : (x[k] + lr);
+                *reinterpret_cast<V*>(W + idx[q]) = Vec4<T>::pack(x);
+            }
+        }
+    }
+}
+
 cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols,
                                     void* W, int w_dtype, int64_t ld, float lr, cudaStream_t s) {
     const int64_t nwords = (rows * cols + 31) / 32;
@@ -360,6 +527,17 @@ cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t
     const int64_t warps_needed = (nwords + 31) / 32;
     const int64_t blocks = (warps_needed + 7) / 8;
     const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
+    const size_t vbytes = w_dtype == MO_F32 ? 16 : 8;
+    const bool vec = cols % 4 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(W) % vbytes) == 0;
+    if (vec) {
+        if (w_dtype == MO_F32)
+            vote_update_vec_kernel<float><<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld,
+                                                               static_cast<float*>(W), lr, nwords);
+        else
+            vote_update_vec_kernel<bf16><<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld,
+                                                              static_cast<bf16*>(W), lr, nwords);
+        return cudaGetLastError();
+    }
     if (w_dtype == MO_F32)
         vote_update_kernel<float><<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld,
                                                        static_cast<float*>(W), lr, nwords);

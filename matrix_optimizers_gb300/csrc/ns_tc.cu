@@ -127,6 +127,32 @@ __device__ __forceinline__ void store32(void* p, int dt, int64_t off, int nv, co
         }
     }
 }
+// fp32 master of X: touched once per phase, so read and written with
+// evict-first hints to leave L2 to the GEMM operands.
+__device__ __forceinline__ void load32_stream(const float* p, int64_t off, int nv, float (&v)[32]) {
+    if (nv == 32) {
+        const float4* s = reinterpret_cast<const float4*>(p + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 x = __ldcs(s + q);
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = k < nv ? __ldcs(p + off + k) : 0.f;
+    }
+}
+__device__ __forceinline__ void store32_stream(float* p, int64_t off, int nv, const float (&v)[32]) {
+    if (nv == 32) {
+        float4* d = reinterpret_cast<float4*>(p + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) __stcs(d + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < nv) __stcs(p + off + k, v[k]);
+    }
+}
 __device__ __forceinline__ float load1(const void* p, int dt, int64_t off) {
     return dt == MO_F32 ? static_cast<const float*>(p)[off] : __bfloat162float(static_cast<const bf16*>(p)[off]);
 }
@@ -205,13 +231,13 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
     } else {
-        load32(md.x_master, MO_F32, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
+        load32_stream(md.x_master, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
     }
     if (p.step + 1 < p.steps) {
         const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
-        store32(md.x_master, MO_F32, off, nv, x);
+        store32_stream(md.x_master, off, nv, x);
         store32(md.x_op[(p.step + 1) & 1], MO_BF16, off, nv, x);
         return;
     }

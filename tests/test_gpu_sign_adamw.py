@@ -29,6 +29,7 @@ def _signed_input(shape, seed):
 
 @pytest.mark.parametrize("shape,ld", [((1, 1), None), ((3, 7), 8), ((5, 33), 40), ((64, 64), None),
                                       ((100, 257), 264), ((1, 4097), None), ((513, 1), 8),
+                                      ((3, 8), None), ((5, 40), 48), ((77, 1000), 1024), ((1, 8), None),
                                       ((2048, 2048), None)])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_sign_pack_bit_exact(shape, ld, dtype):
@@ -46,7 +47,8 @@ def test_sign_pack_bit_exact(shape, ld, dtype):
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 7, 8, 13, 64, 128])
-@pytest.mark.parametrize("shape,ld", [((1, 5), 8), ((33, 95), 96), ((64, 64), None), ((2048, 2048), None)])
+@pytest.mark.parametrize("shape,ld", [((1, 5), 8), ((33, 95), 96), ((64, 64), None), ((7, 12), 16),
+                                      ((31, 100), 104), ((2048, 2048), None)])
 @pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
 def test_vote_update_bit_exact(M, shape, ld, wdtype):
     if M > 13 and shape[0] * shape[1] > 100_000:
