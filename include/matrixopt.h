@@ -183,6 +183,21 @@ int sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
 int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols,
                      void* W, int w_dtype, int64_t ld, float lr, mo_stream_t stream);
 
+/* The int8 all-reduce variant of the vote (SignMuon §2 step 3 "Variante
+ * All-Reduce": an integer-sum all-reduce of the signs, then the local
+ * threshold; 8 bits per element, §2 "Efficienza di Comunicazione").
+ * sign_int8 writes out[j] = -1 if U_j < 0 else +1 (int8) over the row-major
+ * flattening of U (dense, rows*cols bytes; U element-aligned, any ld >= cols).
+ * sign_vote_update_int8 takes a host array of M device pointers to such
+ * buffers (the pre-reduction payloads of M workers), forms each element's
+ * integer sum and applies W <- W - lr*vote with vote = +1 iff sum >= 0 (ties
+ * +1), one fp32 rounding, as sign_vote_update.  1 <= M <= 127 (the int8 sum
+ * range): MO_ERR_INVALID_ARG for M <= 0, MO_ERR_UNSUPPORTED above. */
+int sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
+              int8_t* out, mo_stream_t stream);
+int sign_vote_update_int8(const int8_t* const* signs, int M, int64_t rows, int64_t cols,
+                          void* W, int w_dtype, int64_t ld, float lr, mo_stream_t stream);
+
 /* Owner planner (MatrixFSDP §Metodologia 2), host only.  For matrix i,
  *   bytes_i = rows_i*cols_i*2, flops_i = ns_steps*(4 m^2 n + 2 m^3) (m<=n),
  *   cost_i  = w_bytes*bytes_i/sum(bytes) + w_flops*flops_i/sum(flops);

@@ -76,6 +76,9 @@ _SIGNATURES = [
     ("sign_pack", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     ("sign_vote_update", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
                                    c_int32, c_int64, c_float, c_void_p]),
+    ("sign_int8", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
+    ("sign_vote_update_int8", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
+                                        c_int32, c_int64, c_float, c_void_p]),
     ("plan_owners", c_int32, [ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int32, c_int32,
                               c_int32, c_double, c_double, ctypes.POINTER(c_int32),
                               ctypes.POINTER(c_double)]),
@@ -258,6 +261,20 @@ def sign_vote_update(words, W, lr, stream=None):
     arr = (c_void_p * max(1, M))(*[w.data_ptr() for w in words])
     _check(load().sign_vote_update(arr, M, W.size(0), W.size(1), _ptr(W), dtype_code(W.dtype),
                                    _ld(W), lr, _stream(stream)))
+
+
+def sign_int8(U, out, stream=None):
+    """int8 signs (-1/+1) of U into ``out`` (int8, rows*cols entries)."""
+    _check(load().sign_int8(_ptr(U), dtype_code(U.dtype), U.size(0), U.size(1), _ld(U), _ptr(out),
+                            _stream(stream)))
+
+
+def sign_vote_update_int8(signs, W, lr, stream=None):
+    """W -= lr * sign(sum of the workers' int8 signs), ties -> +1."""
+    M = len(signs)
+    arr = (c_void_p * max(1, M))(*[s.data_ptr() for s in signs])
+    _check(load().sign_vote_update_int8(arr, M, W.size(0), W.size(1), _ptr(W), dtype_code(W.dtype),
+                                        _ld(W), lr, _stream(stream)))
 
 
 def plan_owners(shapes, world, ns_steps=5, w_bytes=1.0, w_flops=1.0):

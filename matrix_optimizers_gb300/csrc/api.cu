@@ -722,6 +722,30 @@ int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t 
     }));
 }
 
+int sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, int8_t* out, mo_stream_t stream) {
+    if (!valid_dtype(dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (ld < cols || U == nullptr || out == nullptr) return MO_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(U) % elem_size(dtype)) != 0) return MO_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return map_cuda(traced(MO_K_PACK, s, [&] { return launch_sign_int8(U, dtype, rows, cols, ld, out, s); }));
+}
+
+int sign_vote_update_int8(const int8_t* const* signs, int M, int64_t rows, int64_t cols, void* W, int w_dtype,
+                          int64_t ld, float lr, mo_stream_t stream) {
+    if (M <= 0 || !valid_dtype(w_dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
+    if (M > 127) return MO_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (signs == nullptr || W == nullptr || ld < cols) return MO_ERR_INVALID_ARG;
+    for (int m = 0; m < M; ++m)
+        if (signs[m] == nullptr) return MO_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) % elem_size(w_dtype)) != 0) return MO_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return map_cuda(traced(MO_K_VOTE, s, [&] {
+        return launch_vote_int8(signs, M, rows, cols, W, w_dtype, ld, lr, s);
+    }));
+}
+
 int plan_owners(const int64_t* rows, const int64_t* cols, int n, int world, int ns_steps, double w_bytes,
                 double w_flops, int32_t* owner_out, double* load_out) {
     if (world <= 0 || n < 0 || ns_steps < 0) return MO_ERR_INVALID_ARG;

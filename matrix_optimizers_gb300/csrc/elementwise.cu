@@ -547,6 +547,139 @@ cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t
     return cudaGetLastError();
 }
 
+// ------------------------------------------------ int8 all-reduce variant
+// sign_int8: out[j] = -1 if U_j < 0 else +1 over the row-major flattening
+// (dense, no padding).  vote_int8: per element, the integer sum of the M
+// workers' int8 signs, vote = +1 iff sum >= 0, W -= lr * vote (one fp32
+// rounding).  Vector paths take 8 (sign) or 16 (vote) elements per thread
+// when such runs lie in one row and are aligned; others go element-wise.
+template <typename T>
+__global__ void __launch_bounds__(256) sign_int8_kernel(const T* __restrict__ U, int64_t rows, int64_t cols,
+                                                        int64_t ld, int8_t* __restrict__ out, int vec) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec) {
+        const int64_t noct = rows * cols / 8, opr = cols / 8;
+        for (int64_t o = first; o < noct; o += stride) {
+            const int64_t r = o / opr, c = (o - r * opr) * 8;
+            float x[8];
+            load8(U + r * ld + c, x);
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                lo |= (x[k] < 0.f ? 0xFFu : 0x01u) << (8 * k);
+                hi |= (x[k + 4] < 0.f ? 0xFFu : 0x01u) << (8 * k);
+            }
+            reinterpret_cast<uint2*>(out)[o] = make_uint2(lo, hi);
+        }
+    } else {
+        const int64_t numel = rows * cols;
+        for (int64_t e = first; e < numel; e += stride) {
+            const int64_t r = e / cols, c = e - r * cols;
+            out[e] = to_float<T>(U[r * ld + c]) < 0.f ? int8_t(-1) : int8_t(1);
+        }
+    }
+}
+
+struct Int8Ptrs {
+    const int8_t* s[kMaxVoters];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) vote_int8_kernel(const __grid_constant__ Int8Ptrs p, int M, int64_t rows,
+                                                        int64_t cols, int64_t ld, T* __restrict__ W, float lr,
+                                                        int vec) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec) {
+        using V = typename Vec4<T>::type;
+        const int64_t ngrp = rows * cols / 16, gpr = cols / 16;
+        for (int64_t g = first; g < ngrp; g += stride) {
+            uint32_t acc[4] = {0, 0, 0, 0};        // 16 signed byte sums (|sum| <= M <= 127)
+            for (int m = 0; m < M; ++m) {
+                const uint4 v = __ldcs(reinterpret_cast<const uint4*>(p.s[m]) + g);
+                acc[0] = __vadd4(acc[0], v.x);
+                acc[1] = __vadd4(acc[1], v.y);
+                acc[2] = __vadd4(acc[2], v.z);
+                acc[3] = __vadd4(acc[3], v.w);
+            }
+            const int64_t r = g / gpr, c = (g - r * gpr) * 16;
+            T* row = W + r * ld + c;
+            V val[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) val[q] = reinterpret_cast<const V*>(row)[q];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float x[4];
+                Vec4<T>::unpack(val[q], x);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const bool neg = (acc[q] >> (8 * k + 7)) & 1u;     // byte sum < 0
+                    x[k] = neg ? (x[k] + lr) : (x[k] - lr);
+                }
+                reinterpret_cast<V*>(row)[q] = Vec4<T>::pack(x);
+            }
+        }
+    } else {
+        const int64_t numel = rows * cols;
+        for (int64_t e = first; e < numel; e += stride) {
+            int sum = 0;
+            for (int m = 0; m < M; ++m) sum += p.s[m][e];
+            const int64_t r = e / cols, c = e - r * cols;
+            const float w = to_float<T>(W[r * ld + c]);
+            const float nv = sum >= 0 ? (w - lr) : (w + lr);
+            if constexpr (sizeof(T) == 4)
+                W[r * ld + c] = nv;
+            else
+                W[r * ld + c] = __float2bfloat16_rn(nv);
+        }
+    }
+}
+
+cudaError_t launch_sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, int8_t* out,
+                             cudaStream_t s) {
+    const int64_t numel = rows * cols;
+    if (numel == 0) return cudaSuccess;
+    const int vec = cols % 8 == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(U) & 15u) == 0 &&
+                    (reinterpret_cast<uintptr_t>(out) & 7u) == 0;
+    const int64_t items = vec ? numel / 8 : numel;
+    int64_t blocks = (items + 255) / 256;
+    const int64_t cap = device_sm_count() * 8LL;
+    if (blocks > cap) blocks = cap;
+    if (dtype == MO_F32)
+        sign_int8_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const float*>(U), rows, cols,
+                                                                         ld, out, vec);
+    else
+        sign_int8_kernel<bf16><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const bf16*>(U), rows, cols, ld,
+                                                                        out, vec);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_vote_int8(const int8_t* const* signs, int M, int64_t rows, int64_t cols, void* W, int w_dtype,
+                             int64_t ld, float lr, cudaStream_t s) {
+    const int64_t numel = rows * cols;
+    if (numel == 0) return cudaSuccess;
+    Int8Ptrs p{};
+    bool aligned = true;
+    for (int m = 0; m < M; ++m) {
+        p.s[m] = signs[m];
+        aligned = aligned && (reinterpret_cast<uintptr_t>(signs[m]) & 15u) == 0;
+    }
+    const size_t vbytes = w_dtype == MO_F32 ? 16 : 8;
+    const int vec = aligned && cols % 16 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(W) % vbytes) == 0;
+    const int64_t items = vec ? numel / 16 : numel;
+    int64_t blocks = (items + 255) / 256;
+    const int64_t cap = device_sm_count() * 8LL;
+    if (blocks > cap) blocks = cap;
+    if (w_dtype == MO_F32)
+        vote_int8_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(p, M, rows, cols, ld, static_cast<float*>(W),
+                                                                         lr, vec);
+    else
+        vote_int8_kernel<bf16><<<static_cast<int>(blocks), 256, 0, s>>>(p, M, rows, cols, ld, static_cast<bf16*>(W),
+                                                                        lr, vec);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------- adamw
 struct AdamArgs {
     float* W; const float* g; float* m; float* v;

@@ -86,6 +86,33 @@ def majority_vote(word_buffers, numel):
     return np.where(2 * c >= M, 1.0, -1.0)
 
 
+def sign_int8(U):
+    """All-reduce variant payload ("Riepilogo Tecnico: SignMuon" §2 step 3,
+    "Variante All-Reduce"; 8 bits per element, §2 "Efficienza di
+    Comunicazione"): the sign of each element as int8 -1/+1, row-major,
+    sign(0) = +1."""
+    return np.where(np.asarray(U, dtype=np.float64).reshape(-1) < 0, -1, 1).astype(np.int8)
+
+
+def int8_vote(sign_buffers):
+    """Integer sum of the workers' int8 signs, then the local threshold
+    sign(sum) with sign(0) = +1 (SignMuon §2 "Meccanismo Principale" item 3)."""
+    total = np.zeros(np.asarray(sign_buffers[0]).size, dtype=np.int64)
+    for s in sign_buffers:
+        total += np.asarray(s, dtype=np.int64)
+    return np.where(total >= 0, 1.0, -1.0)
+
+
+def int8_vote_update(W, sign_buffers, lr, w_dtype="f32"):
+    """W - lr * int8_vote(...), with the same float32 rounding as vote_update."""
+    W = np.asarray(W)
+    vote = int8_vote(sign_buffers).reshape(W.shape).astype(np.float32)
+    new = (W.astype(np.float32) - np.float32(lr) * vote).astype(np.float64)
+    if w_dtype == "bf16":
+        new = round_bf16(new)
+    return new
+
+
 def vote_update(W, word_buffers, lr, w_dtype="f32"):
     """W - lr * vote, one float32 rounding (then bf16 rounding for bf16 W).
 

@@ -113,3 +113,55 @@ def test_adamw_tail_matches_oracle(numel, wd):
     gm, gv = tm_.cpu().numpy().astype(np.float64), tv.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(gm - mr)) <= 16 * 2 ** -24 * np.max(np.abs(mr))
     assert np.max(np.abs(gv - vr) / vr.clip(min=1e-300)) <= 16 * 2 ** -24
+
+
+@pytest.mark.parametrize("shape,ld", [((1, 1), None), ((3, 7), 8), ((5, 40), 48), ((64, 64), None),
+                                      ((33, 95), 96), ((2048, 2048), None)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_sign_int8_bit_exact(shape, ld, dtype):
+    U = _signed_input(shape, sum(shape) + 3)
+    Ut = to_dev(U, dtype, ld)
+    numel = U.size
+    out = torch.full((numel + 16,), 7, dtype=torch.int8, device=dev())      # canary tail
+    mo.sign_int8(Ut, out[:numel])
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(got[:numel], osg.sign_int8(to_np(Ut)))
+    assert np.all(got[numel:] == 7)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 13, 127])
+@pytest.mark.parametrize("shape,ld", [((1, 5), 8), ((33, 95), 96), ((64, 64), None), ((7, 32), 36),
+                                      ((2048, 2048), None)])
+@pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
+def test_int8_vote_update_bit_exact(M, shape, ld, wdtype):
+    if M > 13 and shape[0] * shape[1] > 100_000:
+        pytest.skip("large voter counts are covered on the smaller shapes")
+    rng = np.random.default_rng(M * 7 + shape[1])
+    numel = shape[0] * shape[1]
+    signs = [np.where(rng.random(numel) < 0.5, -1, 1).astype(np.int8) for _ in range(M)]
+    sig_t = [torch.from_numpy(s).to(dev()) for s in signs]
+    W = (0.02 * rng.standard_normal(shape)).astype(np.float32)
+    Wt = to_dev(W, wdtype, ld)
+    W_stored = to_np(Wt)
+    mo.sign_vote_update_int8(sig_t, Wt, 1e-3)
+    torch.cuda.synchronize()
+    want = osg.int8_vote_update(W_stored, signs, 1e-3, "bf16" if wdtype == torch.bfloat16 else "f32")
+    assert np.array_equal(to_np(Wt), want)
+
+
+def test_int8_and_packed_votes_agree_on_gpu():
+    rng = np.random.default_rng(42)
+    U = [rng.standard_normal((256, 512)).astype(np.float32) for _ in range(6)]
+    Ut = [torch.from_numpy(u).to(dev()) for u in U]
+    words = [torch.empty(256 * 512 // 32, dtype=torch.int32, device=dev()) for _ in U]
+    signs = [torch.empty(256 * 512, dtype=torch.int8, device=dev()) for _ in U]
+    for u, w, s in zip(Ut, words, signs):
+        mo.sign_pack(u, w)
+        mo.sign_int8(u, s)
+    W1 = torch.zeros(256, 512, device=dev())
+    W2 = torch.zeros(256, 512, device=dev())
+    mo.sign_vote_update(words, W1, 0.25)
+    mo.sign_vote_update_int8(signs, W2, 0.25)
+    torch.cuda.synchronize()
+    assert torch.equal(W1, W2)

@@ -79,6 +79,25 @@ def test_majority_vote_brute_force_all_patterns(M):
         assert vote[e] == want
 
 
+@pytest.mark.parametrize("M", range(1, 9))
+def test_int8_sum_vote_brute_force_all_patterns(M):
+    pats = list(itertools.product([-1.0, 1.0], repeat=M))
+    S = np.array(pats)
+    signs = [osg.sign_int8(S[:, m]) for m in range(M)]
+    assert all(s.dtype == np.int8 and set(np.unique(s)) <= {-1, 1} for s in signs)
+    vote = osg.int8_vote(signs)
+    for e, pat in enumerate(pats):
+        assert vote[e] == (1.0 if sum(pat) >= 0 else -1.0)
+    # both payloads (1-bit all-gather, int8 all-reduce) give the same vote
+    bufs = [osg.pack_bits(S[:, m]) for m in range(M)]
+    assert np.array_equal(vote, osg.majority_vote(bufs, len(pats)))
+
+
+def test_int8_sign_tie_rule():
+    U = np.array([[-1.0, 0.0, -0.0, np.nan, 2.0, -1e-30]])
+    assert np.array_equal(osg.sign_int8(U), np.array([-1, 1, 1, 1, 1, -1], dtype=np.int8))
+
+
 def test_vote_update_single_float32_rounding():
     rng = np.random.default_rng(3)
     W = rng.standard_normal((9, 13)).astype(np.float32)
