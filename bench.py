@@ -354,8 +354,7 @@ def run_legs(dev, peaks, reps=20):
         return out
 
     def pack_all():
-        for u, w in zip(U, words):
-            mo.sign_pack(u, w)
+        mo.sign_pack_batched(U, words)      # the 8 workers in one launch
 
     pk = graph_ms(pack_all)
     vt = graph_ms(lambda: mo.sign_vote_update(words, W, 1e-3))

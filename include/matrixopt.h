@@ -172,6 +172,12 @@ int ns_orthogonalize_noalloc(const void* X, void* out, int64_t rows, int64_t col
 int sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
               uint32_t* words, mo_stream_t stream);
 
+/* sign_pack for M same-shaped matrices in one launch (the M workers of a
+ * Sign-Muon step): U and words are host arrays of M device pointers, each
+ * pair laid out as for sign_pack.  1 <= M <= 128. */
+int sign_pack_batched(const void* const* U, int M, int dtype, int64_t rows, int64_t cols,
+                      int64_t ld, uint32_t* const* words, mo_stream_t stream);
+
 /* Majority vote over M packed sign buffers and the voted update (SignMuon §2
  * "Meccanismo Principale" item 3 and step 4).  words: host array of M device
  * pointers, each ceil(rows*cols/32) words in sign_pack's layout.  For each

@@ -76,6 +76,8 @@ _SIGNATURES = [
     ("sign_pack", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     ("sign_vote_update", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
                                    c_int32, c_int64, c_float, c_void_p]),
+    ("sign_pack_batched", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int32, c_int64, c_int64, c_int64,
+                                    ctypes.POINTER(c_void_p), c_void_p]),
     ("sign_int8", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     ("sign_vote_update_int8", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
                                         c_int32, c_int64, c_float, c_void_p]),
@@ -261,6 +263,18 @@ def sign_vote_update(words, W, lr, stream=None):
     arr = (c_void_p * max(1, M))(*[w.data_ptr() for w in words])
     _check(load().sign_vote_update(arr, M, W.size(0), W.size(1), _ptr(W), dtype_code(W.dtype),
                                    _ld(W), lr, _stream(stream)))
+
+
+def sign_pack_batched(U, words, stream=None):
+    """sign_pack of M same-shaped matrices (lists U, words) in one launch."""
+    M = len(U)
+    us = (c_void_p * max(1, M))(*[u.data_ptr() for u in U])
+    ws = (c_void_p * max(1, M))(*[w.data_ptr() for w in words])
+    lds = {_ld(u) for u in U}
+    if len(lds) != 1 or len({tuple(u.shape) for u in U}) != 1 or len({u.dtype for u in U}) != 1:
+        raise MoError(MO_ERR_INVALID_ARG, "sign_pack_batched wants one shape, dtype and ld")
+    _check(load().sign_pack_batched(us, M, dtype_code(U[0].dtype), U[0].size(0), U[0].size(1), lds.pop(),
+                                    ws, _stream(stream)))
 
 
 def sign_int8(U, out, stream=None):

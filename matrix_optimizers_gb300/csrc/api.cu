@@ -722,6 +722,24 @@ int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t 
     }));
 }
 
+int sign_pack_batched(const void* const* U, int M, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                      uint32_t* const* words, mo_stream_t stream) {
+    if (M <= 0 || !valid_dtype(dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
+    if (M > 128) return MO_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (ld < cols || U == nullptr || words == nullptr) return MO_ERR_INVALID_ARG;
+    for (int m = 0; m < M; ++m) {
+        if (U[m] == nullptr || words[m] == nullptr) return MO_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(U[m]) % elem_size(dtype)) != 0 ||
+            (reinterpret_cast<uintptr_t>(words[m]) & 3u) != 0)
+            return MO_ERR_ALIGNMENT;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return map_cuda(traced(MO_K_PACK, s, [&] {
+        return launch_sign_pack_batched(U, words, M, dtype, rows, cols, ld, s);
+    }));
+}
+
 int sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, int8_t* out, mo_stream_t stream) {
     if (!valid_dtype(dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return MO_OK;

@@ -293,11 +293,19 @@ __device__ __forceinline__ void load8(const bf16* p, float (&x)[8]) {
     }
 }
 
+constexpr int kMaxPackBatch = 128;
+struct PackPtrs {
+    const void* U[kMaxPackBatch];
+    uint32_t* words[kMaxPackBatch];
+};
+
+// blockIdx.y selects the matrix of a batch (all of one shape).
 template <typename T>
-__global__ void __launch_bounds__(256) sign_pack_vec_kernel(const T* __restrict__ U, int64_t rows, int64_t cols,
-                                                            int64_t ld, uint32_t* __restrict__ words,
-                                                            int64_t nwords) {
+__global__ void __launch_bounds__(256) sign_pack_vec_kernel(const __grid_constant__ PackPtrs pp, int64_t rows,
+                                                            int64_t cols, int64_t ld, int64_t nwords) {
     constexpr int kSub = 4;                       // 4 x 256 elements per warp iteration
+    const T* __restrict__ U = static_cast<const T*>(pp.U[blockIdx.y]);
+    uint32_t* __restrict__ words = pp.words[blockIdx.y];
     const int lane = threadIdx.x & 31;
     const int64_t noct = rows * cols / 8;         // runs of 8 elements
     const int64_t opr = cols / 8;                 // runs per row
@@ -329,23 +337,42 @@ __global__ void __launch_bounds__(256) sign_pack_vec_kernel(const T* __restrict_
     }
 }
 
+cudaError_t launch_sign_pack_batched(const void* const* U, uint32_t* const* words, int M, int dtype, int64_t rows,
+                                     int64_t cols, int64_t ld, cudaStream_t s) {
+    const int64_t nwords = (rows * cols + 31) / 32;
+    if (nwords == 0 || M <= 0) return cudaSuccess;
+    bool vec = cols % 8 == 0 && ld % 8 == 0;
+    for (int m = 0; m < M; ++m) vec = vec && (reinterpret_cast<uintptr_t>(U[m]) & 15u) == 0;
+    if (vec) {
+        PackPtrs pp{};
+        for (int m = 0; m < M; ++m) {
+            pp.U[m] = U[m];
+            pp.words[m] = words[m];
+        }
+        const int64_t warps_needed = (rows * cols / 8 + 127) / 128;
+        const int64_t blocks = (warps_needed + 7) / 8;
+        int64_t cap = device_sm_count() * 8LL / M;
+        if (cap < 1) cap = 1;
+        const dim3 grid(static_cast<unsigned>(blocks < cap ? blocks : cap), static_cast<unsigned>(M));
+        if (dtype == MO_F32)
+            sign_pack_vec_kernel<float><<<grid, 256, 0, s>>>(pp, rows, cols, ld, nwords);
+        else
+            sign_pack_vec_kernel<bf16><<<grid, 256, 0, s>>>(pp, rows, cols, ld, nwords);
+        return cudaGetLastError();
+    }
+    for (int m = 0; m < M; ++m) {
+        cudaError_t e = launch_sign_pack(U[m], dtype, rows, cols, ld, words[m], s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
                              uint32_t* words, cudaStream_t s) {
     const int64_t nwords = (rows * cols + 31) / 32;
     if (nwords == 0) return cudaSuccess;
     const bool vec = cols % 8 == 0 && ld % 8 == 0 && (reinterpret_cast<uintptr_t>(U) & 15u) == 0;
-    if (vec) {
-        const int64_t warps_needed = (rows * cols / 8 + 127) / 128;
-        const int64_t blocks = (warps_needed + 7) / 8;
-        const int grid = static_cast<int>(blocks < device_sm_count() * 8LL ? blocks : device_sm_count() * 8LL);
-        if (dtype == MO_F32)
-            sign_pack_vec_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(U), rows, cols, ld, words,
-                                                             nwords);
-        else
-            sign_pack_vec_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(U), rows, cols, ld, words,
-                                                            nwords);
-        return cudaGetLastError();
-    }
+    if (vec) return launch_sign_pack_batched(&U, &words, 1, dtype, rows, cols, ld, s);
     const int64_t warps_needed = (nwords + kPackWords - 1) / kPackWords;
     const int64_t blocks = (warps_needed + 7) / 8;
     const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
@@ -427,6 +454,7 @@ __global__ void __launch_bounds__(256) vote_update_kernel(const __grid_constant_
 // with ceil(M/2): bit k of the result is 1 when element k votes +1.
 __device__ __forceinline__ uint32_t vote_word(const VotePtrs& ptrs, int M, int nbits, uint32_t thr, int64_t w) {
     uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll 8
     for (int m = 0; m < M; ++m) {
         uint32_t x = __ldcs(ptrs.w[m] + w);
 #pragma unroll
@@ -488,7 +516,7 @@ __global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_const
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t base = warp * 32; base < nwords; base += nwarps * 32) {
-        const uint32_t plus = base + lane < nwords ? vote_word(ptrs, M, nbits, thr, base + lane) : 0u;
+        // W loads first, so they are in flight with the word loads below
         int64_t e = base * 32 + 4 * lane;
         int64_t r = e / cols, c = e - r * cols;
         int64_t idx[8];
@@ -500,6 +528,7 @@ __global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_const
             c += 128;
             while (c >= cols) { c -= cols; ++r; }
         }
+        const uint32_t plus = base + lane < nwords ? vote_word(ptrs, M, nbits, thr, base + lane) : 0u;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const uint32_t vw = __shfl_sync(0xffffffffu, plus, 4 * q + (lane >> 3));

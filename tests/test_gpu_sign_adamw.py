@@ -165,3 +165,18 @@ def test_int8_and_packed_votes_agree_on_gpu():
     mo.sign_vote_update_int8(signs, W2, 0.25)
     torch.cuda.synchronize()
     assert torch.equal(W1, W2)
+
+
+@pytest.mark.parametrize("shape,ld", [((64, 64), None), ((5, 40), 48), ((33, 95), 96), ((2048, 2048), None)])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_sign_pack_batched_bit_exact(shape, ld, M):
+    Us = [_signed_input(shape, 100 + m) for m in range(M)]
+    Ut = [to_dev(u, torch.bfloat16, ld) for u in Us]
+    nw = (Us[0].size + 31) // 32
+    words = [torch.full((nw + 4,), -1, dtype=torch.int32, device=dev()) for _ in range(M)]
+    mo.sign_pack_batched(Ut, [w[:nw] for w in words])
+    torch.cuda.synchronize()
+    for u, w in zip(Ut, words):
+        got = _words_np(w)
+        assert np.array_equal(got[:nw], osg.pack_bits(to_np(u)))
+        assert np.all(got[nw:] == 0xFFFFFFFF)
