@@ -189,6 +189,18 @@ int sign_pack_batched(const void* const* U, int M, int dtype, int64_t rows, int6
 int sign_vote_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols,
                      void* W, int w_dtype, int64_t ld, float lr, mo_stream_t stream);
 
+/* The optional local polar step on the vote (SignMuon §2 "Flusso
+ * Algoritmico" step 5): the voted sign matrix S_bar (+1/-1, majority of the M
+ * packed buffers, ties +1) is orthogonalised locally with the quintic
+ * Newton-Schulz iteration (bf16 tensor cores, k = steps, X0 = S_bar/||S_bar||_F)
+ * and W <- W - lr * NS(S_bar).  W follows the 16-byte rules of
+ * muon_step_batched; ws (256-byte aligned) holds S_bar and the NS buffers,
+ * sized by sign_vote_polar_workspace_bytes (host only).  1 <= M <= 128. */
+int sign_vote_polar_workspace_bytes(int64_t rows, int64_t cols, int64_t ld, size_t* bytes_out);
+int sign_vote_polar_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols,
+                           void* W, int w_dtype, int64_t ld, float lr, int steps,
+                           float a, float b, float c, void* ws, size_t ws_bytes, mo_stream_t stream);
+
 /* The int8 all-reduce variant of the vote (SignMuon §2 step 3 "Variante
  * All-Reduce": an integer-sum all-reduce of the signs, then the local
  * threshold; 8 bits per element, §2 "Efficienza di Comunicazione").

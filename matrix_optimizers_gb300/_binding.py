@@ -76,6 +76,10 @@ _SIGNATURES = [
     ("sign_pack", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     ("sign_vote_update", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
                                    c_int32, c_int64, c_float, c_void_p]),
+    ("sign_vote_polar_workspace_bytes", c_int32, [c_int64, c_int64, c_int64, ctypes.POINTER(c_size_t)]),
+    ("sign_vote_polar_update", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p, c_int32,
+                                         c_int64, c_float, c_int32, c_float, c_float, c_float, c_void_p,
+                                         c_size_t, c_void_p]),
     ("sign_pack_batched", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int32, c_int64, c_int64, c_int64,
                                     ctypes.POINTER(c_void_p), c_void_p]),
     ("sign_int8", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
@@ -263,6 +267,21 @@ def sign_vote_update(words, W, lr, stream=None):
     arr = (c_void_p * max(1, M))(*[w.data_ptr() for w in words])
     _check(load().sign_vote_update(arr, M, W.size(0), W.size(1), _ptr(W), dtype_code(W.dtype),
                                    _ld(W), lr, _stream(stream)))
+
+
+def sign_vote_polar_workspace_bytes(W):
+    out = c_size_t(0)
+    _check(load().sign_vote_polar_workspace_bytes(W.size(0), W.size(1), _ld(W), ctypes.byref(out)))
+    return out.value
+
+
+def sign_vote_polar_update(words, W, lr, ws, steps=5, a=3.4445, b=-4.7750, c=2.0315, stream=None):
+    """W -= lr * NS(majority_vote(words)): the vote followed by the local polar step."""
+    M = len(words)
+    arr = (c_void_p * max(1, M))(*[w.data_ptr() for w in words])
+    _check(load().sign_vote_polar_update(arr, M, W.size(0), W.size(1), _ptr(W), dtype_code(W.dtype), _ld(W),
+                                         lr, steps, a, b, c, _ptr(ws), ws.numel() if ws is not None else 0,
+                                         _stream(stream)))
 
 
 def sign_pack_batched(U, words, stream=None):

@@ -740,6 +740,68 @@ int sign_pack_batched(const void* const* U, int M, int dtype, int64_t rows, int6
     }));
 }
 
+int sign_vote_polar_workspace_bytes(int64_t rows, int64_t cols, int64_t ld, size_t* bytes_out) {
+    if (bytes_out == nullptr) return MO_ERR_INVALID_ARG;
+    int st = validate_dims(rows, cols, ld);
+    if (st != MO_OK) return st;
+    if (rows == 0 || cols == 0) {
+        *bytes_out = 0;
+        return MO_OK;
+    }
+    const size_t sbytes = align_up(static_cast<size_t>(rows) * ld * 2, kBufAlign);
+    *bytes_out = sbytes + make_layout({{rows, cols}}, MO_NS_BF16).total;
+    return MO_OK;
+}
+
+int sign_vote_polar_update(const uint32_t* const* words, int M, int64_t rows, int64_t cols, void* W, int w_dtype,
+                           int64_t ld, float lr, int steps, float a, float b, float c, void* ws, size_t ws_bytes,
+                           mo_stream_t stream) {
+    if (M <= 0 || !valid_dtype(w_dtype) || steps < 0) return MO_ERR_INVALID_ARG;
+    if (M > 128) return MO_ERR_UNSUPPORTED;
+    int st = validate_dims(rows, cols, ld);
+    if (st != MO_OK) return st;
+    if (rows == 0 || cols == 0) return MO_OK;
+    if (words == nullptr) return MO_ERR_INVALID_ARG;
+    for (int m = 0; m < M; ++m) {
+        if (words[m] == nullptr) return MO_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(words[m]) & 3u) != 0) return MO_ERR_ALIGNMENT;
+    }
+    if ((st = validate_buffer(W, w_dtype, ld)) != MO_OK) return st;
+    size_t need = 0;
+    sign_vote_polar_workspace_bytes(rows, cols, ld, &need);
+    if ((st = validate_ws(ws, ws_bytes, need)) != MO_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // S_bar (bf16, W's layout) at the start of the workspace, the NS workspace after it
+    void* S = ws;
+    const size_t sbytes = align_up(static_cast<size_t>(rows) * ld * 2, kBufAlign);
+    cudaError_t e = traced(MO_K_VOTE, s, [&] { return launch_vote_matrix(words, M, rows, cols, S, ld, s); });
+    if (e != cudaSuccess) return MO_ERR_CUDA;
+    Job j;
+    j.rows = rows;
+    j.cols = cols;
+    j.ld = ld;
+    j.src_dtype = MO_BF16;
+    j.g_dtype = MO_BF16;
+    j.w_dtype = w_dtype;
+    j.out_dtype = w_dtype;
+    j.has_momentum = 0;
+    j.src = S;
+    j.grad = nullptr;
+    j.W = W;
+    j.out = nullptr;
+    NsOpts o;
+    o.precision = MO_NS_BF16;
+    o.steps = steps;
+    o.apply_update = 1;
+    o.mu = 0.f;
+    o.a = a;
+    o.b = b;
+    o.c = c;
+    o.alpha = lr;
+    o.decay = 0.f;
+    return run_ns({j}, o, static_cast<uint8_t*>(ws) + sbytes, ws_bytes - sbytes, s);
+}
+
 int sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, int8_t* out, mo_stream_t stream) {
     if (!valid_dtype(dtype) || rows < 0 || cols < 0) return MO_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return MO_OK;

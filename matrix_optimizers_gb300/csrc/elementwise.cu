@@ -576,6 +576,47 @@ cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ vote_matrix
+// The voted sign matrix itself, S_bar = +1 / -1 as bf16, written in a
+// rows x cols layout with leading dimension ld (input of the optional local
+// polar step).  Element-wise over words, coalesced along the flattening.
+__global__ void __launch_bounds__(256) vote_matrix_kernel(const __grid_constant__ VotePtrs ptrs, int M, int nbits,
+                                                          uint32_t thr, int64_t rows, int64_t cols, int64_t ld,
+                                                          bf16* __restrict__ S, int64_t nwords) {
+    const int lane = threadIdx.x & 31;
+    const int64_t numel = rows * cols;
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const bf16 plus1 = __float2bfloat16_rn(1.f), minus1 = __float2bfloat16_rn(-1.f);
+    for (int64_t base = warp * 32; base < nwords; base += nwarps * 32) {
+        const uint32_t plus = base + lane < nwords ? vote_word(ptrs, M, nbits, thr, base + lane) : 0u;
+        int64_t e = base * 32 + lane;
+        int64_t r = e / cols, c = e - r * cols;
+        for (int q = 0; q < 32; ++q) {
+            const uint32_t vw = __shfl_sync(0xffffffffu, plus, q);
+            if (e < numel) S[r * ld + c] = ((vw >> lane) & 1u) ? plus1 : minus1;
+            e += 32;
+            c += 32;
+            while (c >= cols) { c -= cols; ++r; }
+        }
+    }
+}
+
+cudaError_t launch_vote_matrix(const uint32_t* const* words, int M, int64_t rows, int64_t cols, void* S, int64_t ld,
+                               cudaStream_t s) {
+    const int64_t nwords = (rows * cols + 31) / 32;
+    if (nwords == 0) return cudaSuccess;
+    VotePtrs ptrs{};
+    for (int m = 0; m < M; ++m) ptrs.w[m] = words[m];
+    int nbits = 0;
+    while ((1 << nbits) <= M) ++nbits;
+    const uint32_t thr = static_cast<uint32_t>((M + 1) / 2);
+    const int64_t blocks = ((nwords + 31) / 32 + 7) / 8;
+    const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
+    vote_matrix_kernel<<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld, static_cast<bf16*>(S), nwords);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------ int8 all-reduce variant
 // sign_int8: out[j] = -1 if U_j < 0 else +1 over the row-major flattening
 // (dense, no padding).  vote_int8: per element, the integer sum of the M

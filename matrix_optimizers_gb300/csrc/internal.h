@@ -109,6 +109,8 @@ cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t
 cudaError_t launch_adamw(const mo_adamw_tail& t, cudaStream_t s);
 cudaError_t launch_sign_pack_batched(const void* const* U, uint32_t* const* words, int M, int dtype, int64_t rows,
                                      int64_t cols, int64_t ld, cudaStream_t s);
+cudaError_t launch_vote_matrix(const uint32_t* const* words, int M, int64_t rows, int64_t cols, void* S, int64_t ld,
+                               cudaStream_t s);
 cudaError_t launch_sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, int8_t* out,
                              cudaStream_t s);
 cudaError_t launch_vote_int8(const int8_t* const* signs, int M, int64_t rows, int64_t cols, void* W, int w_dtype,

@@ -8,13 +8,14 @@
 // kGram and kPoly compute only the 128 x 256 tiles that meet the upper
 // triangle (j >= i) and store each upper element at (i, j) and (j, i).
 //
-// Roles per CTA (320 threads, one CTA per SM):
-//   warps 0-7  epilogue: tcgen05.ld of the fp32 accumulator, fused math,
-//              global stores; warp w reads TMEM lanes 32*(w%4).. and column
-//              half w/4 of the 256-column accumulator;
-//   warp 8     TMA producer: 64 x 64 bf16 boxes (128-byte swizzle) into a
+// Roles per CTA (576 threads, one CTA per SM):
+//   warps 0-15 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
+//              global stores; warp w reads TMEM lanes 32*(w%4).. and the
+//              64-column slice w/4 of the 256-column accumulator (16 warps
+//              keep the memory-heavy apply epilogue shorter than a main loop);
+//   warp 16    TMA producer: 64 x 64 bf16 boxes (128-byte swizzle) into a
 //              4-stage shared-memory ring (48 KB per stage);
-//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
+//   warp 17    TMEM allocator and single-thread tcgen05.mma issuer
 //              (M = 128, N = 256, K = 16 per instruction) into a double-
 //              buffered accumulator (2 x 256 TMEM columns), so the epilogue
 //              of one tile overlaps the main loop of the next.
@@ -39,16 +40,13 @@ constexpr int kBoxBytes = kBox * kBox * 2;                 // 8 KB
 constexpr int kABytes = kTcBM * kTcBK * 2;                 // 16 KB
 constexpr int kBBytes = kTcBN * kTcBK * 2;                 // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kEpiWarps = 8;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kEpiWarps = 16;                              // 4 lane quarters x 4 column slices
+constexpr int kEpiSliceCols = kTcBN / (kEpiWarps / 4);     // 64 accumulator columns per epilogue warp
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr uint32_t kTmemCols = 512;
-constexpr int kCtlBytes = 1024;                            // barriers, TMEM address, abort flag
-constexpr int kEpiBufBytesAll = kEpiWarps * 32 * 33 * 4;   // per-warp 32 x 33 fp32 transpose blocks
-// ring + control + epilogue blocks + worst-case 1 KB alignment slack = 227 KB
-constexpr int kSmemBytes = kStages * kStageBytes + kCtlBytes + kEpiBufBytesAll + 1024;
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of dynamic shared memory per CTA");
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
 
 struct Ctl {
     uint64_t full[kStages];
@@ -59,9 +57,104 @@ struct Ctl {
     uint32_t tmem_base;
     int abort_flag;
 };
-static_assert(sizeof(Ctl) <= kCtlBytes, "control block overflows its shared-memory slot");
 
 // ---------------------------------------------------------------- helpers
+__device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = __low2float(h[q]);
+        v[2 * q + 1] = __high2float(h[q]);
+    }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
+    uint4 u;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+        w[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return u;
+}
+
+// 32 consecutive elements starting at p[off]; `nv` of them valid.  A full
+// group is read with 16-byte vector loads (offsets are 32-element aligned
+// and leading dimensions 16-byte multiples).
+__device__ __forceinline__ void load32(const void* p, int dt, int64_t off, int nv, float (&v)[32]) {
+    if (nv == 32) {
+        if (dt == MO_F32) {
+            const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = s[q];
+                v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+            }
+        } else {
+            const uint4* s = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) unpack_bf16x8(s[q], &v[8 * q]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            float x = 0.f;
+            if (k < nv)
+                x = dt == MO_F32 ? static_cast<const float*>(p)[off + k]
+                                 : __bfloat162float(static_cast<const bf16*>(p)[off + k]);
+            v[k] = x;
+        }
+    }
+}
+__device__ __forceinline__ void store32(void* p, int dt, int64_t off, int nv, const float (&v)[32]) {
+    if (nv == 32) {
+        if (dt == MO_F32) {
+            float4* d = reinterpret_cast<float4*>(static_cast<float*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+            uint4* d = reinterpret_cast<uint4*>(static_cast<bf16*>(p) + off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) d[q] = pack_bf16x8(&v[8 * q]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (k < nv) {
+                if (dt == MO_F32)
+                    static_cast<float*>(p)[off + k] = v[k];
+                else
+                    static_cast<bf16*>(p)[off + k] = __float2bfloat16_rn(v[k]);
+            }
+        }
+    }
+}
+// fp32 master of X: touched once per phase, so read and written with
+// evict-first hints to leave L2 to the GEMM operands.
+__device__ __forceinline__ void load32_stream(const float* p, int64_t off, int nv, float (&v)[32]) {
+    if (nv == 32) {
+        const float4* s = reinterpret_cast<const float4*>(p + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 x = __ldcs(s + q);
+            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = k < nv ? __ldcs(p + off + k) : 0.f;
+    }
+}
+__device__ __forceinline__ void store32_stream(float* p, int64_t off, int nv, const float (&v)[32]) {
+    if (nv == 32) {
+        float4* d = reinterpret_cast<float4*>(p + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) __stcs(d + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < nv) __stcs(p + off + k, v[k]);
+    }
+}
 __device__ __forceinline__ float load1(const void* p, int dt, int64_t off) {
     return dt == MO_F32 ? static_cast<const float*>(p)[off] : __bfloat162float(static_cast<const bf16*>(p)[off]);
 }
@@ -72,154 +165,93 @@ __device__ __forceinline__ void store1(void* p, int dt, int64_t off, float v) {
         static_cast<bf16*>(p)[off] = __float2bfloat16_rn(v);
 }
 
-// ------------------------------------------------------------- epilogues
-// The accumulator arrives in "row layout": lane l of a warp holds row
-// rowbase + l, columns j0 .. j0+31.  Global accesses along a row are
-// coalesced in "column layout" (lane l holds column j0 + l of rows
-// rowbase .. rowbase+31), reached by a 32 x 32 transpose through the warp's
-// shared-memory block (33-float rows: conflict-free both ways).  Accesses
-// that run down a column of the user matrix (mirror stores, transposed
-// matrices) stay in row layout, where consecutive lanes touch consecutive
-// addresses.  Both epilogues are called by all 32 lanes (warp-uniform).
-constexpr int kEpiPitch = 33;
-constexpr int kEpiBufBytes = 32 * kEpiPitch * 4;
-
-__device__ __forceinline__ void transpose32(float* buf, const float (&in)[32], float (&out)[32]) {
-    const int lane = threadIdx.x & 31;
-    __syncwarp();
+// Oriented access to a user matrix: X(i, j) = U(i, j), or U(j, i) when the
+// matrix was transposed to reach m <= n.  Transposed accesses are per
+// element; across a warp (consecutive i) they are contiguous.
+__device__ __forceinline__ void user_load32(const MatDesc& md, const void* p, int dt, int i, int j0, int nv,
+                                            float (&v)[32]) {
+    if (!md.transposed) {
+        load32(p, dt, static_cast<int64_t>(i) * md.ld + j0, nv, v);
+    } else {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) buf[lane * kEpiPitch + k] = in[k];
-    __syncwarp();
+        for (int k = 0; k < 32; ++k) v[k] = k < nv ? load1(p, dt, static_cast<int64_t>(j0 + k) * md.ld + i) : 0.f;
+    }
+}
+__device__ __forceinline__ void user_store32(const MatDesc& md, void* p, int dt, int i, int j0, int nv,
+                                             const float (&v)[32]) {
+    if (!md.transposed) {
+        store32(p, dt, static_cast<int64_t>(i) * md.ld + j0, nv, v);
+    } else {
 #pragma unroll
-    for (int r = 0; r < 32; ++r) out[r] = buf[r * kEpiPitch + lane];
+        for (int k = 0; k < 32; ++k)
+            if (k < nv) store1(p, dt, static_cast<int64_t>(j0 + k) * md.ld + i, v[k]);
+    }
 }
 
+// ------------------------------------------------------------- epilogues
 // Symmetric phases: keep elements with j >= i, store at (i, j) and (j, i).
-__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int rowbase, int j0,
-                                              float (&v)[32], float* buf) {
-    const int m = md.m, lane = threadIdx.x & 31;
-    if (j0 + 31 < rowbase || j0 >= m || rowbase >= m) return;     // block wholly below the diagonal / outside
+__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int i, int j0,
+                                              float (&v)[32]) {
+    const int m = md.m;
+    if (j0 + 31 < i || j0 >= m) return;
     bf16* dst = static_cast<bf16*>(p.phase == kGram ? md.gram : md.poly);
-    const int jc = j0 + lane;                                        // column-layout column
-    float c[32];
+    const int nv = min(32, m - j0);
     if (p.phase == kGram) {
         const float sc = p.step == 0 ? md.scales[1] : 1.f;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] *= sc;
-        transpose32(buf, v, c);
     } else {
-        transpose32(buf, v, c);
-        const bf16* A = static_cast<const bf16*>(md.gram);
         float a[32];
+        load32(md.gram, MO_BF16, static_cast<int64_t>(i) * md.lda + j0, nv, a);
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = rowbase + r;
-            a[r] = (i < m && jc < m) ? __bfloat162float(A[static_cast<int64_t>(i) * md.lda + jc]) : 0.f;
-        }
+        for (int k = 0; k < 32; ++k) v[k] = fmaf(p.c, v[k], p.b * a[k]);
+    }
+    const int64_t row = static_cast<int64_t>(i) * md.lda;
+    if (j0 >= i) {
+        store32(dst, MO_BF16, row + j0, nv, v);
+    } else {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) c[r] = fmaf(p.c, c[r], p.b * a[r]);
-        transpose32(buf, c, v);                                      // back to row layout for the mirror
+        for (int k = 0; k < 32; ++k)
+            if (j0 + k >= i && k < nv) dst[row + j0 + k] = __float2bfloat16_rn(v[k]);
     }
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {                                   // (i, j), j >= i: along rows
-        const int i = rowbase + r;
-        if (i < m && jc < m && jc >= i) dst[static_cast<int64_t>(i) * md.lda + jc] = __float2bfloat16_rn(c[r]);
-    }
-    const int ir = rowbase + lane;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {                                   // (j, i), j > i: down columns
+    for (int k = 0; k < 32; ++k) {
         const int j = j0 + k;
-        if (ir < m && j < m && j > ir) dst[static_cast<int64_t>(j) * md.lda + ir] = __float2bfloat16_rn(v[k]);
+        if (j > i && k < nv) dst[static_cast<int64_t>(j) * md.lda + i] = __float2bfloat16_rn(v[k]);
     }
 }
 
-__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int rowbase, int j0,
-                                          float (&v)[32], float* buf) {
-    const int m = md.m, n = md.n, lane = threadIdx.x & 31;
-    if (j0 >= n || rowbase >= m) return;
-    const int jc = j0 + lane;
-    const bool col_ok = jc < n;
-    const int ir = rowbase + lane;
-    float x[32];                                                     // column layout
-    if (p.step == 0 && md.transposed) {
-        // X(i, j) = M(j, i): read M down its columns in row layout
-        float s[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-            s[k] = (ir < m && j0 + k < n) ? load1(md.src, md.src_dtype, static_cast<int64_t>(j0 + k) * md.ld + ir)
-                                          : 0.f;
+__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int i, int j0,
+                                          float (&v)[32]) {
+    const int n = md.n;
+    if (j0 >= n) return;
+    const int nv = min(32, n - j0);
+    float x[32];
+    if (p.step == 0) {
+        user_load32(md, md.src, md.src_dtype, i, j0, nv, x);
         const float inv_s = md.scales[0];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = inv_s * fmaf(p.a, s[k], v[k]);
-        transpose32(buf, s, x);
+        for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
     } else {
-        transpose32(buf, v, x);
-        float s[32];
-        if (p.step == 0) {
+        load32_stream(md.x_master, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const int i = rowbase + r;
-                s[r] = (i < m && col_ok) ? load1(md.src, md.src_dtype, static_cast<int64_t>(i) * md.ld + jc) : 0.f;
-            }
-            const float inv_s = md.scales[0];
-#pragma unroll
-            for (int r = 0; r < 32; ++r) x[r] = inv_s * fmaf(p.a, s[r], x[r]);
-        } else {
-#pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const int i = rowbase + r;
-                s[r] = (i < m && col_ok) ? __ldcs(md.x_master + static_cast<int64_t>(i) * md.ldx + jc) : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < 32; ++r) x[r] = fmaf(p.a, s[r], x[r]);
-        }
+        for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
     }
     if (p.step + 1 < p.steps) {
-        bf16* xb = static_cast<bf16*>(md.x_op[(p.step + 1) & 1]);
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = rowbase + r;
-            if (i < m && col_ok) {
-                const int64_t o = static_cast<int64_t>(i) * md.ldx + jc;
-                __stcs(md.x_master + o, x[r]);
-                xb[o] = __float2bfloat16_rn(x[r]);
-            }
-        }
+        const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
+        store32_stream(md.x_master, off, nv, x);
+        store32(md.x_op[(p.step + 1) & 1], MO_BF16, off, nv, x);
         return;
     }
-    void* dst = p.apply_update ? md.W : md.out;
-    if (dst == nullptr) return;
-    const int dt = p.apply_update ? md.w_dtype : md.out_dtype;
-    if (!md.transposed) {
+    if (p.apply_update) {
+        if (md.W == nullptr) return;
         float w[32];
-        if (p.apply_update) {
+        user_load32(md, md.W, md.w_dtype, i, j0, nv, w);
 #pragma unroll
-            for (int r = 0; r < 32; ++r) {
-                const int i = rowbase + r;
-                w[r] = (i < m && col_ok) ? load1(dst, dt, static_cast<int64_t>(i) * md.ld + jc) : 0.f;
-            }
-#pragma unroll
-            for (int r = 0; r < 32; ++r) x[r] = fmaf(-p.alpha, x[r], w[r] - p.decay * w[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int i = rowbase + r;
-            if (i < m && col_ok) store1(dst, dt, static_cast<int64_t>(i) * md.ld + jc, x[r]);
-        }
-    } else {
-        float xr[32];                                                // row layout: X(ir, j0 + k) = U(j0 + k, ir)
-        transpose32(buf, x, xr);
-        if (p.apply_update) {
-            float w[32];
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                w[k] = (ir < m && j0 + k < n) ? load1(dst, dt, static_cast<int64_t>(j0 + k) * md.ld + ir) : 0.f;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) xr[k] = fmaf(-p.alpha, xr[k], w[k] - p.decay * w[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-            if (ir < m && j0 + k < n) store1(dst, dt, static_cast<int64_t>(j0 + k) * md.ld + ir, xr[k]);
+        for (int k = 0; k < 32; ++k) w[k] = fmaf(-p.alpha, x[k], w[k] - p.decay * w[k]);
+        user_store32(md, md.W, md.w_dtype, i, j0, nv, w);
+    } else if (md.out != nullptr) {
+        user_store32(md, md.out, md.out_dtype, i, j0, nv, x);
     }
 }
 
@@ -350,8 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < kWaitCycles) {}
         }
     } else {
-        const int quarter = warp & 3, half = warp >> 2;
-        float* buf = reinterpret_cast<float*>(smem + kStages * kStageBytes + kCtlBytes + warp * kEpiBufBytes);
+        const int quarter = warp & 3, slice = warp >> 2;
         for (int t = 0; t < range.y; ++t) {
             const TileDesc td = p.tiles[range.x + t];
             const MatDesc& md = p.mats[td.mat];
@@ -360,24 +391,27 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             const bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104);
             if (!__all_sync(0xffffffffu, ok)) break;                     // warp-uniform exit
             tc_fence_after();
-            const int rowbase = td.ti * kTcBM + quarter * 32;
+            const int i = td.ti * kTcBM + quarter * 32 + lane;
+            const bool row_ok = i < md.m;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                const int col = half * 128 + ch * 32;
+            for (int ch = 0; ch < kEpiSliceCols / 32; ++ch) {
+                const int col = slice * kEpiSliceCols + ch * 32;
                 uint32_t r[32];
                 __syncwarp();
                 tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(acc * kTcBN + col),
                                    r);
                 tmem_wait_ld();
-                float v[32];
+                if (row_ok) {
+                    float v[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-                const int j0 = td.tj * kTcBN + col;
-                if (p.phase == kApply)
-                    epi_apply(p, md, rowbase, j0, v, buf);
-                else
-                    epi_symmetric(p, md, rowbase, j0, v, buf);
+                    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+                    const int j0 = td.tj * kTcBN + col;
+                    if (p.phase == kApply)
+                        epi_apply(p, md, i, j0, v);
+                    else
+                        epi_symmetric(p, md, i, j0, v);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -113,6 +113,17 @@ def int8_vote_update(W, sign_buffers, lr, w_dtype="f32"):
     return new
 
 
+def vote_polar_update(W, word_buffers, lr, steps=5, a=3.4445, b=-4.7750, c=2.0315):
+    """The optional local polar step (SignMuon §2 "Flusso Algoritmico" step
+    5): the voted sign matrix S_bar is orthogonalised locally with the same
+    Newton-Schulz iteration before the update, W <- W - lr * NS(S_bar).
+    Returns float64 W (no storage rounding)."""
+    from .muon import newton_schulz
+    W = np.asarray(W, dtype=np.float64)
+    S = majority_vote(word_buffers, W.size).reshape(W.shape)
+    return W - lr * newton_schulz(S, steps, a, b, c)
+
+
 def vote_update(W, word_buffers, lr, w_dtype="f32"):
     """W - lr * vote, one float32 rounding (then bf16 rounding for bf16 W).
 

@@ -180,3 +180,24 @@ def test_sign_pack_batched_bit_exact(shape, ld, M):
         got = _words_np(w)
         assert np.array_equal(got[:nw], osg.pack_bits(to_np(u)))
         assert np.all(got[nw:] == 0xFFFFFFFF)
+
+
+@pytest.mark.parametrize("shape,ld", [((256, 512), None), ((512, 256), None), ((200, 300), 304),
+                                      ((2048, 2048), None)])
+@pytest.mark.parametrize("M", [3, 8])
+def test_vote_polar_update_vs_oracle(shape, ld, M):
+    """The local polar step on the vote: W - lr * NS(S_bar) within the bf16 NS tolerance."""
+    from tests.gpu_helpers import NS_BF16_TOL, rel_fro, workspace
+    rng = np.random.default_rng(M + shape[0])
+    numel = shape[0] * shape[1]
+    bufs = [osg.pack_bits(rng.standard_normal(shape)) for _ in range(M)]
+    words = [torch.from_numpy(b.view(np.int32).copy()).to(dev()) for b in bufs]
+    W = (0.02 * rng.standard_normal(shape)).astype(np.float32)
+    Wt = to_dev(W, torch.float32, ld)
+    W0 = to_np(Wt)
+    ws = workspace(mo.sign_vote_polar_workspace_bytes(Wt))
+    mo.sign_vote_polar_update(words, Wt, 1e-2, ws)
+    torch.cuda.synchronize()
+    want = osg.vote_polar_update(W0, bufs, 1e-2)
+    assert rel_fro(to_np(Wt) - W0, want - W0) < NS_BF16_TOL
+    assert numel == W.size

@@ -93,6 +93,21 @@ def test_int8_sum_vote_brute_force_all_patterns(M):
     assert np.array_equal(vote, osg.majority_vote(bufs, len(pats)))
 
 
+def test_vote_polar_update_composes_vote_and_closed_form_ns():
+    rng = np.random.default_rng(21)
+    shape = (12, 20)
+    bufs = [osg.pack_bits(rng.standard_normal(shape)) for _ in range(5)]
+    W = rng.standard_normal(shape)
+    got = osg.vote_polar_update(W, bufs, 0.1)
+    S = osg.majority_vote(bufs, W.size).reshape(shape)
+    U, s, Vt = np.linalg.svd(S / np.linalg.norm(S), full_matrices=False)
+    for _ in range(5):
+        s = 3.4445 * s - 4.7750 * s ** 3 + 2.0315 * s ** 5
+    np.testing.assert_allclose(got, W - 0.1 * (U * s) @ Vt, atol=1e-12)
+    # ||S_bar||_F = sqrt(numel): every entry is +-1
+    assert np.linalg.norm(S) == np.sqrt(S.size)
+
+
 def test_int8_sign_tie_rule():
     U = np.array([[-1.0, 0.0, -0.0, np.nan, 2.0, -1e-30]])
     assert np.array_equal(osg.sign_int8(U), np.array([-1, 1, 1, 1, 1, -1], dtype=np.int8))
