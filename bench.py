@@ -482,6 +482,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-matrices", type=int, default=0,
                     help="step only the first N matrices of the set (small profiling cases)")
+    ap.add_argument("--apply-operand", choices=["kmajor", "mn"], default="kmajor",
+                    help="B operand of the NS apply phase: K-major X^T copy (default) or X via MN-major")
     args = ap.parse_args()
     if args.impl == "gb300" and args.warmup < 3:
         args.warmup = 3
@@ -499,8 +501,11 @@ def main():
         tdist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
         dist = tdist
     import matrix_optimizers_gb300 as mo
+    from matrix_optimizers_gb300 import _binding
     mo.load()
+    _binding.mo_debug_set_apply_operand(1 if args.apply_operand == "kmajor" else 0)
     res = run_gb300(args, rank, world, local_rank, dist)
+    res["config"]["apply_operand"] = args.apply_operand
     if rank == 0:
         print(json.dumps(res), flush=True)
     if dist is not None:

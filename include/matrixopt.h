@@ -121,6 +121,19 @@ int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg,
                       const mo_adamw_tail* tail, void* const* out,
                       void* ws, size_t ws_bytes, mo_stream_t stream);
 
+/* A Sign-Muon worker's step with the sign extraction and 1-bit packing
+ * fused into the last Newton-Schulz epilogue (SignMuon §2 "Flusso
+ * Algoritmico" steps 1-3): momentum and NS as muon_step_batched, no weight
+ * update, and instead of the direction U the packed words of sign(U) are
+ * written to words[i] (host array of n device pointers, ceil(rows*cols/32)
+ * uint32 each, sign_pack's layout and tie rule).  The sign is taken of U as
+ * stored in cfg->out_dtype, so the words equal sign_pack of the output
+ * muon_step_batched would write.  bf16 NS only, ns_steps >= 1, and every
+ * matrix's cols a multiple of 32 (else MO_ERR_UNSUPPORTED); ws sized by
+ * mo_workspace_bytes. */
+int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg,
+                          uint32_t* const* words, void* ws, size_t ws_bytes, mo_stream_t stream);
+
 /* Workspace size for ns_orthogonalize on these shapes (host only). */
 int ns_workspace_bytes(const int64_t* rows, const int64_t* cols, int n,
                        int precision, size_t* bytes_out);

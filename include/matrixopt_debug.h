@@ -46,6 +46,12 @@ int mo_debug_sm_count(void);
  * affects launches issued after the call. */
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
+/* Source of the apply phase's B operand (bf16 mode): 1 (default) reads a
+ * K-major bf16 copy of X^T that the momentum kernel and each apply epilogue
+ * also write; 0 reads X itself through an MN-major descriptor.  Both give
+ * identical results; process-wide, for measurement. */
+int mo_debug_set_apply_operand(int kmajor);
+
 /* Launch tracing, for measurement.  mo_trace_enable(capacity) makes every
  * later kernel launch of the calling thread (any entry point) record a CUDA
  * event before and after it on the call's stream, for up to `capacity`

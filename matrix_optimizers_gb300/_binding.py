@@ -65,6 +65,8 @@ _SIGNATURES = [
     ("muon_step_batched", c_int32, [ctypes.POINTER(mo_matrix), c_int32, ctypes.POINTER(mo_muon_cfg),
                                     ctypes.POINTER(mo_adamw_tail), ctypes.POINTER(c_void_p),
                                     c_void_p, c_size_t, c_void_p]),
+    ("muon_step_sign_packed", c_int32, [ctypes.POINTER(mo_matrix), c_int32, ctypes.POINTER(mo_muon_cfg),
+                                        ctypes.POINTER(c_void_p), c_void_p, c_size_t, c_void_p]),
     ("ns_workspace_bytes", c_int32, [ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int32, c_int32,
                                      ctypes.POINTER(c_size_t)]),
     ("ns_orthogonalize", c_int32, [ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
@@ -95,6 +97,7 @@ _SIGNATURES = [
                                    c_int32, ctypes.POINTER(mo_ns_view)]),
     ("mo_debug_sm_count", c_int32, []),
     ("mo_debug_set_mn_strides", c_int32, [ctypes.c_uint32, ctypes.c_uint32]),
+    ("mo_debug_set_apply_operand", c_int32, [c_int32]),
     ("mo_trace_enable", c_int32, [c_int32]),
     ("mo_trace_read", c_int32, [ctypes.POINTER(c_int32), ctypes.POINTER(c_float), c_int32,
                                 ctypes.POINTER(c_int32)]),
@@ -211,6 +214,14 @@ def muon_step_batched(mats, cfg, ws, tail=None, out=None, stream=None):
         _mat_array(mats), len(mats), ctypes.byref(cfg),
         ctypes.byref(tail) if tail is not None else None, outs,
         _ptr(ws), ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def muon_step_sign_packed(mats, cfg, words, ws, stream=None):
+    """Sign-Muon worker step: momentum + NS with the packed signs of the
+    direction written to ``words`` (list of int32 tensors) in the last epilogue."""
+    arr = (c_void_p * max(1, len(words)))(*[w.data_ptr() for w in words])
+    _check(load().muon_step_sign_packed(_mat_array(mats), len(mats), ctypes.byref(cfg), arr, _ptr(ws),
+                                        ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def ns_workspace_bytes(shapes, precision=MO_NS_BF16):
@@ -337,6 +348,10 @@ def mo_debug_ns_view(shapes, index, precision=MO_NS_BF16):
 
 def mo_debug_set_mn_strides(lbo, sbo):
     _check(load().mo_debug_set_mn_strides(lbo, sbo))
+
+
+def mo_debug_set_apply_operand(kmajor):
+    _check(load().mo_debug_set_apply_operand(int(kmajor)))
 
 
 def mo_trace_enable(capacity):

@@ -84,6 +84,8 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 // 8-row K groups of 1 KB).  Exposed to tests through the debug header.
 std::atomic<uint32_t> g_mn_lbo{8192};
 std::atomic<uint32_t> g_mn_sbo{1024};
+// Apply-phase B operand: 1 = K-major from the X^T copy, 0 = MN-major from X.
+std::atomic<int> g_apply_kmajor{1};
 
 // ------------------------------------------------------------- the request
 struct Job {
@@ -94,6 +96,7 @@ struct Job {
     const void* grad;
     void* W;
     void* out;
+    uint32_t* words = nullptr;   // fused sign + pack target (muon_step_sign_packed)
 };
 
 struct Shape {
@@ -112,7 +115,7 @@ Shape oriented(int64_t rows, int64_t cols) {
 }
 
 struct MatBufs {
-    size_t x_op[2], x_master, gram, poly;
+    size_t x_op[2], xt_op[2], x_master, gram, poly;
 };
 
 // Counts of tiles per phase for one matrix.
@@ -163,7 +166,7 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
     L.mats = off;
     off = align_up(off + n * sizeof(MatDesc), 128);
     L.tmaps = off;
-    if (precision == MO_NS_BF16) off = align_up(off + n * 4 * sizeof(CUtensorMap), 128);
+    if (precision == MO_NS_BF16) off = align_up(off + n * 6 * sizeof(CUtensorMap), 128);
     for (int ph = 0; ph < 3; ++ph) {
         L.tiles[ph] = off;
         off = align_up(off + static_cast<size_t>(L.ntiles[ph]) * sizeof(TileDesc), 128);
@@ -187,8 +190,12 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
         if (precision == MO_NS_BF16) {
             b.x_master = off;
             off = align_up(off + static_cast<size_t>(s.m) * s.ldx * 4, kBufAlign);
+            const size_t xtbytes = static_cast<size_t>(s.n) * s.lda * 2;      // X^T: n x lda bf16
+            b.xt_op[0] = off; off = align_up(off + xtbytes, kBufAlign);
+            b.xt_op[1] = off; off = align_up(off + xtbytes, kBufAlign);
         } else {
             b.x_master = 0;
+            b.xt_op[0] = b.xt_op[1] = 0;
         }
         b.gram = off; off = align_up(off + abytes, kBufAlign);
         b.poly = off; off = align_up(off + abytes, kBufAlign);
@@ -304,7 +311,7 @@ std::vector<int64_t> plan_key(const std::vector<Job>& jobs, int precision, const
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     std::vector<int64_t> k;
-    k.reserve(4 + jobs.size() * 12);
+    k.reserve(4 + jobs.size() * 13);
     k.push_back(dev);
     k.push_back(precision);
     k.push_back(static_cast<int64_t>(reinterpret_cast<uintptr_t>(ws)));
@@ -316,6 +323,7 @@ std::vector<int64_t> plan_key(const std::vector<Job>& jobs, int precision, const
                                static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.W)),
                                static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.out))};
         k.insert(k.end(), f, f + 12);
+        k.push_back(static_cast<int64_t>(reinterpret_cast<uintptr_t>(j.words)));
     }
     return k;
 }
@@ -361,6 +369,7 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
         d.grad = j.grad;
         d.W = j.W;
         d.out = j.out;
+        d.sign_words = j.words;
         d.x_op[0] = base + b.x_op[0];
         d.x_op[1] = base + b.x_op[1];
         d.x_master = o.precision == MO_NS_BF16 ? reinterpret_cast<float*>(base + b.x_master) : nullptr;
@@ -372,16 +381,21 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
         d.mom_tiles_c = static_cast<int32_t>(ceil_div(j.cols, kMomTile));
         mom_begin += static_cast<int64_t>(d.mom_tiles_r) * d.mom_tiles_c;
         if (o.precision == MO_NS_BF16) {
+            d.xt_op[0] = base + b.xt_op[0];
+            d.xt_op[1] = base + b.xt_op[1];
             for (int q = 0; q < 2; ++q) {
-                if (!encode_bf16_map(&htm[4 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
-                d.tm_x[q] = dtm + 4 * i + q;
+                if (!encode_bf16_map(&htm[6 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
+                d.tm_x[q] = dtm + 6 * i + q;
+                if (!encode_bf16_map(&htm[6 * i + 4 + q], d.xt_op[q], s.n, s.m, s.lda)) return MO_ERR_CUDA;
+                d.tm_xt[q] = dtm + 6 * i + 4 + q;
             }
-            if (!encode_bf16_map(&htm[4 * i + 2], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            if (!encode_bf16_map(&htm[4 * i + 3], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            d.tm_gram = dtm + 4 * i + 2;
-            d.tm_poly = dtm + 4 * i + 3;
+            if (!encode_bf16_map(&htm[6 * i + 2], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&htm[6 * i + 3], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            d.tm_gram = dtm + 6 * i + 2;
+            d.tm_poly = dtm + 6 * i + 3;
         } else {
-            d.tm_x[0] = d.tm_x[1] = d.tm_gram = d.tm_poly = nullptr;
+            d.xt_op[0] = d.xt_op[1] = nullptr;
+            d.tm_x[0] = d.tm_x[1] = d.tm_xt[0] = d.tm_xt[1] = d.tm_gram = d.tm_poly = nullptr;
         }
     }
 
@@ -486,6 +500,8 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     mp.ntiles = L.mom_tiles;
     mp.mu = o.mu;
     mp.fp32_operand = o.precision == MO_NS_FP32;
+    const int kmajor = o.precision == MO_NS_BF16 && g_apply_kmajor.load() != 0;
+    mp.write_xt = kmajor && o.steps > 0;
     mp.partials = reinterpret_cast<float*>(base + L.partials);
     const int mom_grid = static_cast<int>(std::min<int64_t>(L.mom_tiles, static_cast<int64_t>(nsm) * 8));
     e = traced(MO_K_MOMENTUM, stream, [&] { return launch_momentum_norm(mp, mom_grid, stream); });
@@ -510,6 +526,7 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     np.decay = o.decay;
     np.mn_lbo = g_mn_lbo.load();
     np.mn_sbo = g_mn_sbo.load();
+    np.b_kmajor = kmajor;
     for (int t = 0; t < o.steps; ++t) {
         for (int ph = 0; ph < 3; ++ph) {
             np.phase = ph;
@@ -517,7 +534,7 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
             np.tiles = reinterpret_cast<const TileDesc*>(base + L.tiles[ph]);
             np.cta_range = reinterpret_cast<const int2*>(base + L.ranges[ph]);
             np.ntiles = static_cast<int32_t>(L.ntiles[ph]);
-            np.idesc = idesc_bf16_f32(kTcBM, kTcBN, ph == kApply ? 1u : 0u);
+            np.idesc = idesc_bf16_f32(kTcBM, kTcBN, (ph == kApply && !kmajor) ? 1u : 0u);
             e = traced(MO_K_GRAM + ph, stream, [&] {
                 return o.precision == MO_NS_BF16 ? launch_ns_tc_phase(np, grids[ph], stream)
                                                  : launch_ns_fp32_phase(np, grids[ph], stream);
@@ -637,6 +654,42 @@ int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, cons
     o.alpha = cfg->lr * cfg->update_scale;
     o.decay = cfg->lr * cfg->weight_decay;
     return run_ns(jobs, o, ws, ws_bytes, s);
+}
+
+int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, uint32_t* const* words, void* ws,
+                          size_t ws_bytes, mo_stream_t stream) {
+    if (cfg == nullptr) return MO_ERR_INVALID_ARG;
+    if (cfg->ns_precision != MO_NS_BF16 || cfg->ns_steps < 1) return MO_ERR_UNSUPPORTED;
+    mo_muon_cfg c2 = *cfg;
+    c2.apply_update = 0;
+    std::vector<Job> jobs;
+    std::vector<int> idx;
+    int st = gather_muon_jobs(mats, n, &c2, nullptr, false, jobs, &idx);
+    if (st != MO_OK) return st;
+    if (!jobs.empty() && words == nullptr) return MO_ERR_INVALID_ARG;
+    for (size_t k = 0; k < jobs.size(); ++k) {
+        const mo_matrix& mt = mats[idx[k]];
+        if ((st = validate_buffer(mt.M, mt.m_dtype, mt.ld)) != MO_OK) return st;
+        if ((st = validate_buffer(mt.G, mt.g_dtype, mt.ld)) != MO_OK) return st;
+        uint32_t* w = words[idx[k]];
+        if (w == nullptr) return MO_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(w) & 3u) != 0) return MO_ERR_ALIGNMENT;
+        if (mt.cols % 32 != 0) return MO_ERR_UNSUPPORTED;    // rows must start on word boundaries
+        jobs[k].words = w;
+        jobs[k].W = nullptr;
+        jobs[k].out = nullptr;
+    }
+    NsOpts o;
+    o.precision = MO_NS_BF16;
+    o.steps = cfg->ns_steps;
+    o.apply_update = 0;
+    o.mu = cfg->mu;
+    o.a = cfg->a;
+    o.b = cfg->b;
+    o.c = cfg->c;
+    o.alpha = 0.f;
+    o.decay = 0.f;
+    return run_ns(jobs, o, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int ns_workspace_bytes(const int64_t* rows, const int64_t* cols, int n, int precision, size_t* bytes_out) {
@@ -920,6 +973,12 @@ int mo_debug_sm_count(void) {
     int c = 0;
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return c;
+}
+
+int mo_debug_set_apply_operand(int kmajor) {
+    if (kmajor != 0 && kmajor != 1) return MO_ERR_INVALID_ARG;
+    g_apply_kmajor.store(kmajor);
+    return MO_OK;
 }
 
 int mo_trace_enable(int capacity) {

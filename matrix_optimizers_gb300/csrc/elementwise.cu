@@ -119,17 +119,24 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) ss = fmaf(x[k], x[k], ss);
+                // the user's own orientation: X itself, or X^T for a transposed matrix
                 if (!md.transposed)
                     store4(md.x_op[0], op_dt, static_cast<int64_t>(r) * md.ldx + c, nvalid, x);
+                else if (p.write_xt)
+                    store4(md.xt_op[0], MO_BF16, static_cast<int64_t>(r) * md.lda + c, nvalid, x);
             }
-            if (md.transposed) {
+            if (md.transposed || p.write_xt) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) tileT[4 * col4 + k][rl] = x[k];
             }
         }
-        if (md.transposed) {
+        if (md.transposed || p.write_xt) {
             __syncthreads();
-            // oriented row xr = user column c0 + xr; oriented columns r0 + seg .. +15
+            // the other orientation through the tile transpose: row xr = user
+            // column c0 + xr, columns = user rows r0 + seg .. +15
+            void* dst = md.transposed ? md.x_op[0] : md.xt_op[0];
+            const int dt = md.transposed ? op_dt : MO_BF16;
+            const int64_t dld = md.transposed ? md.ldx : md.lda;
             const int xr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;
             const int orow = c0 + xr;
             if (orow < md.cols) {
@@ -141,7 +148,7 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
                         float v[4];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) v[k] = tileT[xr][seg + 4 * g4 + k];
-                        store4(md.x_op[0], op_dt, static_cast<int64_t>(orow) * md.ldx + ocol, nv, v);
+                        store4(dst, dt, static_cast<int64_t>(orow) * dld + ocol, nv, v);
                     }
                 }
             }

@@ -221,11 +221,47 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
     }
 }
 
-__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int i, int j0,
+// Fused Sign-Muon sign + 1-bit pack of the last step's output: bit = 1
+// unless the output, as stored in out_dtype, is below zero; bits follow the
+// row-major flattening of the user matrix, whose column count is a multiple
+// of 32, so every word is written whole by one warp.
+__device__ __forceinline__ bool sign_bit(float v, int out_dtype) {
+    if (out_dtype == MO_BF16) v = __bfloat162float(__float2bfloat16_rn(v));
+    return !(v < 0.f);
+}
+
+__device__ __forceinline__ void epi_sign_pack(const MatDesc& md, int i, bool row_ok, int j0, int nv,
+                                              const float (&x)[32]) {
+    const int lane = threadIdx.x & 31;
+    if (!md.transposed) {
+        // the lane's 32 columns are one word of its row
+        if (!row_ok) return;
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+            if (k < nv && sign_bit(x[k], md.out_dtype)) w |= 1u << k;
+        md.sign_words[(static_cast<int64_t>(i) * md.cols + j0) >> 5] = w;
+    } else {
+        // lanes are 32 consecutive user columns: one ballot per user row j0 + k
+        uint32_t mine = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const uint32_t w = __ballot_sync(0xffffffffu, row_ok && k < nv && sign_bit(x[k], md.out_dtype));
+            if (lane == k) mine = w;
+        }
+        const int rowbase = i - lane;
+        if (rowbase < md.m && lane < nv)
+            md.sign_words[(static_cast<int64_t>(j0 + lane) * md.cols + rowbase) >> 5] = mine;
+    }
+}
+
+// Called by all 32 lanes of a warp (the fused pack takes warp ballots);
+// lanes whose row lies beyond the matrix touch no memory.
+__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int i, bool row_ok, int j0,
                                           float (&v)[32]) {
     const int n = md.n;
     if (j0 >= n) return;
-    const int nv = min(32, n - j0);
+    const int nv = row_ok ? min(32, n - j0) : 0;
     float x[32];
     if (p.step == 0) {
         user_load32(md, md.src, md.src_dtype, i, j0, nv, x);
@@ -238,11 +274,25 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
         for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
     }
     if (p.step + 1 < p.steps) {
+        if (!row_ok) return;
         const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
         store32_stream(md.x_master, off, nv, x);
         store32(md.x_op[(p.step + 1) & 1], MO_BF16, off, nv, x);
+        if (p.b_kmajor) {
+            // X^T for the next apply's K-major B operand: down columns, so
+            // consecutive lanes (rows i) write consecutive addresses
+            bf16* xt = static_cast<bf16*>(md.xt_op[(p.step + 1) & 1]);
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (k < nv) xt[static_cast<int64_t>(j0 + k) * md.lda + i] = __float2bfloat16_rn(x[k]);
+        }
         return;
     }
+    if (md.sign_words != nullptr) {
+        epi_sign_pack(md, i, row_ok, j0, min(32, n - j0), x);
+        return;
+    }
+    if (!row_ok) return;
     if (p.apply_update) {
         if (md.W == nullptr) return;
         float w[32];
@@ -286,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     const int2 range = p.cta_range[blockIdx.x];
-    const bool mn_b = p.phase == kApply;
+    const bool mn_b = p.phase == kApply && !p.b_kmajor;
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -306,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     tma = tmb = md.tm_gram;
                 } else {
                     tma = md.tm_poly;
-                    tmb = md.tm_x[p.step & 1];
+                    tmb = p.b_kmajor ? md.tm_xt[p.step & 1] : md.tm_x[p.step & 1];
                 }
                 for (int kb = 0; kb < td.nkb; ++kb) {
                     const uint32_t empty = smem_u32(&ctl->empty[stage]);
@@ -402,16 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                                        static_cast<uint32_t>(acc * kTcBN + col),
                                    r);
                 tmem_wait_ld();
-                if (row_ok) {
-                    float v[32];
+                float v[32];
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-                    const int j0 = td.tj * kTcBN + col;
-                    if (p.phase == kApply)
-                        epi_apply(p, md, i, j0, v);
-                    else
-                        epi_symmetric(p, md, i, j0, v);
-                }
+                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+                const int j0 = td.tj * kTcBN + col;
+                if (p.phase == kApply)
+                    epi_apply(p, md, i, row_ok, j0, v);
+                else if (row_ok)
+                    epi_symmetric(p, md, i, j0, v);
             }
             tc_fence_before();
             __syncwarp();

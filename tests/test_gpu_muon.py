@@ -158,6 +158,48 @@ def test_sign_muon_m8_step_bit_exact_vote():
     assert np.array_equal(to_np(W), osg.vote_update(W0, ref_words, c["lr"]))
 
 
+@pytest.mark.parametrize("shapes", [[(256, 512), (512, 256)], [(96, 160), (160, 96), (2048, 2048)],
+                                    [(200, 64), (64, 200), (320, 320)]])
+def test_sign_packed_step_equals_separate_pack(shapes):
+    """Fused sign + pack in the last NS epilogue == sign_pack of the bf16
+    direction written by the unfused step, bit for bit."""
+    rng = np.random.default_rng(len(shapes))
+    G = [rng.standard_normal(s).astype(np.float32) for s in shapes]
+    cfg_out = mo.make_cfg(mu=0.95, apply_update=False, out_dtype=mo.MO_BF16)
+
+    def fresh():
+        Ms = [torch.zeros(s, dtype=torch.bfloat16, device=dev()) for s in shapes]
+        Gs = [torch.from_numpy(g).to(dev()) for g in G]
+        return Ms, Gs, [mo.make_matrix(m, m, g) for m, g in zip(Ms, Gs)]
+
+    Ms, Gs, mats = fresh()
+    U = [torch.zeros(s, dtype=torch.bfloat16, device=dev()) for s in shapes]
+    ws = workspace(mo.mo_workspace_bytes(mats, cfg_out))
+    mo.muon_step_batched(mats, cfg_out, ws, out=U)
+    ref = [torch.empty((s[0] * s[1] + 31) // 32, dtype=torch.int32, device=dev()) for s in shapes]
+    for u, w in zip(U, ref):
+        mo.sign_pack(u, w)
+    Ms2, Gs2, mats2 = fresh()
+    fused = [torch.full_like(w, -7) for w in ref]
+    mo.muon_step_sign_packed(mats2, cfg_out, fused, ws)
+    torch.cuda.synchronize()
+    for a, b, s in zip(fused, ref, shapes):
+        assert torch.equal(a, b), s
+    for m1, m2 in zip(Ms, Ms2):
+        assert torch.equal(m1, m2)                       # same momentum state update
+
+
+def test_sign_packed_step_rejects_unaligned_columns():
+    M = torch.zeros(64, 40, device=dev())
+    G = torch.ones(64, 40, device=dev())
+    words = [torch.empty(80, dtype=torch.int32, device=dev())]
+    cfg = mo.make_cfg(apply_update=False)
+    ws = workspace(mo.mo_workspace_bytes([mo.make_matrix(M, M, G)], cfg))
+    with pytest.raises(mo.MoError) as e:
+        mo.muon_step_sign_packed([mo.make_matrix(M, M, G)], cfg, words, ws)
+    assert e.value.status == -6
+
+
 @pytest.mark.slow
 def test_llama7b_owner0_sampled():
     c = CONFIGS["llama7b_owner0"]
