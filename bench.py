@@ -136,6 +136,31 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def _sm_balance(st):
+    """Load balance of the NS launches across SMs from per-CTA %globaltimer
+    stamps: per launch, the busiest CTA's time over the mean CTA time."""
+    if len(st) == 0:
+        return None
+    ratios, sum_max, sum_mean, spans = [], 0.0, 0.0, []
+    for launch in st:
+        ok = launch[:, 1] > 0
+        if not ok.any():
+            continue
+        busy = (launch[ok, 1] - launch[ok, 0]).astype(np.float64)
+        ratios.append(float(busy.max() / busy.mean()))
+        sum_max += float(busy.max())
+        sum_mean += float(busy.mean())
+        spans.append(float(launch[ok, 1].max() - launch[ok, 0].min()))
+    phases = {}
+    for k, r in enumerate(ratios):
+        phases.setdefault(("gram", "poly", "apply")[k % 3], []).append(r)
+    return {"launches": len(ratios), "ctas_per_launch_max": int(st.shape[1]),
+            "max_over_mean_busy": sum_max / sum_mean,
+            "per_launch_median": float(np.median(ratios)), "per_launch_worst": float(np.max(ratios)),
+            "per_phase_median": {k: float(np.median(v)) for k, v in phases.items()},
+            "metric": "busiest CTA time / mean CTA time per NS launch (1.0 = perfect), from %globaltimer stamps"}
+
+
 def _shape_summary(shapes):
     from collections import Counter
     c = Counter(tuple(s) for s in shapes)
@@ -201,6 +226,11 @@ def run_gb300(args, rank, world, local_rank, dist):
     if mo.mo_check_device_status(ws) != 0:
         raise SystemExit("device status error after warm-up")
 
+    from matrix_optimizers_gb300 import _binding
+    n_ns = 3 * 5 * args.steps
+    max_ctas = torch.cuda.get_device_properties(dev).multi_processor_count
+    stamps = torch.zeros(2 * n_ns * max_ctas, dtype=torch.int64, device=dev)
+    _binding.mo_debug_cta_stamps(stamps, n_ns, max_ctas)
     mo.mo_trace_enable(64 * (args.steps + 1))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
@@ -216,6 +246,8 @@ def run_gb300(args, rank, world, local_rank, dist):
         dist.barrier()
     trace = mo.mo_trace_read()
     mo.mo_trace_enable(0)
+    recorded = _binding.mo_debug_cta_stamps(None, 0, 0)
+    sm_balance = _sm_balance(stamps.view(n_ns, max_ctas, 2).cpu().numpy()[:recorded])
     status = mo.mo_check_device_status(ws)
     ms_step = _max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)
     total_mats = _sum_over_ranks(float(len(shapes)), dist)
@@ -262,6 +294,7 @@ def run_gb300(args, rank, world, local_rank, dist):
         },
         "kernels": {k: {"launches": v[0], "total_ms": v[1], "share": v[1] / max(1e-9, all_ms)}
                     for k, v in by_kind.items()},
+        "sm_balance": sm_balance,
         "gpu_launches": len(trace), "launches_per_step": len(trace) // max(1, args.steps),
         "device_status": status,
     }
@@ -482,8 +515,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--max-matrices", type=int, default=0,
                     help="step only the first N matrices of the set (small profiling cases)")
-    ap.add_argument("--apply-operand", choices=["kmajor", "mn"], default="kmajor",
-                    help="B operand of the NS apply phase: K-major X^T copy (default) or X via MN-major")
     args = ap.parse_args()
     if args.impl == "gb300" and args.warmup < 3:
         args.warmup = 3
@@ -501,11 +532,8 @@ def main():
         tdist.init_process_group("gloo", init_method="env://", rank=rank, world_size=world)
         dist = tdist
     import matrix_optimizers_gb300 as mo
-    from matrix_optimizers_gb300 import _binding
     mo.load()
-    _binding.mo_debug_set_apply_operand(1 if args.apply_operand == "kmajor" else 0)
     res = run_gb300(args, rank, world, local_rank, dist)
-    res["config"]["apply_operand"] = args.apply_operand
     if rank == 0:
         print(json.dumps(res), flush=True)
     if dist is not None:

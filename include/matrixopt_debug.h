@@ -46,11 +46,14 @@ int mo_debug_sm_count(void);
  * affects launches issued after the call. */
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
-/* Source of the apply phase's B operand (bf16 mode): 1 (default) reads a
- * K-major bf16 copy of X^T that the momentum kernel and each apply epilogue
- * also write; 0 reads X itself through an MN-major descriptor.  Both give
- * identical results; process-wide, for measurement. */
-int mo_debug_set_apply_operand(int kmajor);
+/* SM load-balance record.  With a device buffer `buf` of
+ * 2 * capacity * max_ctas uint64 values, each of the calling thread's next
+ * `capacity` tensor-core Newton-Schulz launches (grid <= max_ctas) has CTA c
+ * write its start and end %globaltimer (ns) to buf[2*(k*max_ctas + c)] and
+ * [.. + 1], k counting launches from 0.  *recorded (nullable) receives the
+ * number of launches recorded since the previous call.  buf = NULL stops
+ * recording.  Measurement only: no effect on results. */
+int mo_debug_cta_stamps(uint64_t* buf, int capacity, int max_ctas, int* recorded);
 
 /* Launch tracing, for measurement.  mo_trace_enable(capacity) makes every
  * later kernel launch of the calling thread (any entry point) record a CUDA

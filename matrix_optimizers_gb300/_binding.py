@@ -97,7 +97,7 @@ _SIGNATURES = [
                                    c_int32, ctypes.POINTER(mo_ns_view)]),
     ("mo_debug_sm_count", c_int32, []),
     ("mo_debug_set_mn_strides", c_int32, [ctypes.c_uint32, ctypes.c_uint32]),
-    ("mo_debug_set_apply_operand", c_int32, [c_int32]),
+    ("mo_debug_cta_stamps", c_int32, [c_void_p, c_int32, c_int32, ctypes.POINTER(c_int32)]),
     ("mo_trace_enable", c_int32, [c_int32]),
     ("mo_trace_read", c_int32, [ctypes.POINTER(c_int32), ctypes.POINTER(c_float), c_int32,
                                 ctypes.POINTER(c_int32)]),
@@ -350,8 +350,13 @@ def mo_debug_set_mn_strides(lbo, sbo):
     _check(load().mo_debug_set_mn_strides(lbo, sbo))
 
 
-def mo_debug_set_apply_operand(kmajor):
-    _check(load().mo_debug_set_apply_operand(int(kmajor)))
+def mo_debug_cta_stamps(buf, capacity, max_ctas):
+    """Start recording per-CTA start/end stamps into ``buf`` (int64 CUDA
+    tensor of 2*capacity*max_ctas entries); ``buf=None`` stops.  Returns the
+    number of launches recorded since the previous call."""
+    rec = c_int32(0)
+    _check(load().mo_debug_cta_stamps(_ptr(buf), capacity, max_ctas, ctypes.byref(rec)))
+    return rec.value
 
 
 def mo_trace_enable(capacity):

@@ -84,8 +84,6 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 // 8-row K groups of 1 KB).  Exposed to tests through the debug header.
 std::atomic<uint32_t> g_mn_lbo{8192};
 std::atomic<uint32_t> g_mn_sbo{1024};
-// Apply-phase B operand: 1 = K-major from the X^T copy, 0 = MN-major from X.
-std::atomic<int> g_apply_kmajor{1};
 
 // ------------------------------------------------------------- the request
 struct Job {
@@ -115,7 +113,7 @@ Shape oriented(int64_t rows, int64_t cols) {
 }
 
 struct MatBufs {
-    size_t x_op[2], xt_op[2], x_master, gram, poly;
+    size_t x_op[2], x_master, gram, poly;
 };
 
 // Counts of tiles per phase for one matrix.
@@ -166,7 +164,7 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
     L.mats = off;
     off = align_up(off + n * sizeof(MatDesc), 128);
     L.tmaps = off;
-    if (precision == MO_NS_BF16) off = align_up(off + n * 6 * sizeof(CUtensorMap), 128);
+    if (precision == MO_NS_BF16) off = align_up(off + n * 4 * sizeof(CUtensorMap), 128);
     for (int ph = 0; ph < 3; ++ph) {
         L.tiles[ph] = off;
         off = align_up(off + static_cast<size_t>(L.ntiles[ph]) * sizeof(TileDesc), 128);
@@ -190,12 +188,8 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
         if (precision == MO_NS_BF16) {
             b.x_master = off;
             off = align_up(off + static_cast<size_t>(s.m) * s.ldx * 4, kBufAlign);
-            const size_t xtbytes = static_cast<size_t>(s.n) * s.lda * 2;      // X^T: n x lda bf16
-            b.xt_op[0] = off; off = align_up(off + xtbytes, kBufAlign);
-            b.xt_op[1] = off; off = align_up(off + xtbytes, kBufAlign);
         } else {
             b.x_master = 0;
-            b.xt_op[0] = b.xt_op[1] = 0;
         }
         b.gram = off; off = align_up(off + abytes, kBufAlign);
         b.poly = off; off = align_up(off + abytes, kBufAlign);
@@ -277,6 +271,15 @@ struct Trace {
     std::vector<int32_t> kind;
 };
 thread_local Trace t_trace;
+
+// Optional per-CTA start / end stamps of the tensor-core NS launches
+// (mo_debug_cta_stamps): launch k of the record writes 2 * max_ctas values
+// at buf + 2 * k * max_ctas.
+struct Stamps {
+    unsigned long long* buf = nullptr;
+    int capacity = 0, max_ctas = 0, count = 0;
+};
+thread_local Stamps t_stamps;
 
 template <typename F>
 cudaError_t traced(int kind, cudaStream_t s, F&& launch) {
@@ -381,21 +384,16 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
         d.mom_tiles_c = static_cast<int32_t>(ceil_div(j.cols, kMomTile));
         mom_begin += static_cast<int64_t>(d.mom_tiles_r) * d.mom_tiles_c;
         if (o.precision == MO_NS_BF16) {
-            d.xt_op[0] = base + b.xt_op[0];
-            d.xt_op[1] = base + b.xt_op[1];
             for (int q = 0; q < 2; ++q) {
-                if (!encode_bf16_map(&htm[6 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
-                d.tm_x[q] = dtm + 6 * i + q;
-                if (!encode_bf16_map(&htm[6 * i + 4 + q], d.xt_op[q], s.n, s.m, s.lda)) return MO_ERR_CUDA;
-                d.tm_xt[q] = dtm + 6 * i + 4 + q;
+                if (!encode_bf16_map(&htm[4 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
+                d.tm_x[q] = dtm + 4 * i + q;
             }
-            if (!encode_bf16_map(&htm[6 * i + 2], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            if (!encode_bf16_map(&htm[6 * i + 3], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            d.tm_gram = dtm + 6 * i + 2;
-            d.tm_poly = dtm + 6 * i + 3;
+            if (!encode_bf16_map(&htm[4 * i + 2], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&htm[4 * i + 3], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            d.tm_gram = dtm + 4 * i + 2;
+            d.tm_poly = dtm + 4 * i + 3;
         } else {
-            d.xt_op[0] = d.xt_op[1] = nullptr;
-            d.tm_x[0] = d.tm_x[1] = d.tm_xt[0] = d.tm_xt[1] = d.tm_gram = d.tm_poly = nullptr;
+            d.tm_x[0] = d.tm_x[1] = d.tm_gram = d.tm_poly = nullptr;
         }
     }
 
@@ -500,8 +498,6 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     mp.ntiles = L.mom_tiles;
     mp.mu = o.mu;
     mp.fp32_operand = o.precision == MO_NS_FP32;
-    const int kmajor = o.precision == MO_NS_BF16 && g_apply_kmajor.load() != 0;
-    mp.write_xt = kmajor && o.steps > 0;
     mp.partials = reinterpret_cast<float*>(base + L.partials);
     const int mom_grid = static_cast<int>(std::min<int64_t>(L.mom_tiles, static_cast<int64_t>(nsm) * 8));
     e = traced(MO_K_MOMENTUM, stream, [&] { return launch_momentum_norm(mp, mom_grid, stream); });
@@ -526,7 +522,6 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     np.decay = o.decay;
     np.mn_lbo = g_mn_lbo.load();
     np.mn_sbo = g_mn_sbo.load();
-    np.b_kmajor = kmajor;
     for (int t = 0; t < o.steps; ++t) {
         for (int ph = 0; ph < 3; ++ph) {
             np.phase = ph;
@@ -534,7 +529,11 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
             np.tiles = reinterpret_cast<const TileDesc*>(base + L.tiles[ph]);
             np.cta_range = reinterpret_cast<const int2*>(base + L.ranges[ph]);
             np.ntiles = static_cast<int32_t>(L.ntiles[ph]);
-            np.idesc = idesc_bf16_f32(kTcBM, kTcBN, (ph == kApply && !kmajor) ? 1u : 0u);
+            np.idesc = idesc_bf16_f32(kTcBM, kTcBN, ph == kApply ? 1u : 0u);
+            np.stamps = nullptr;
+            Stamps& sp = t_stamps;
+            if (o.precision == MO_NS_BF16 && sp.buf != nullptr && sp.count < sp.capacity && grids[ph] <= sp.max_ctas)
+                np.stamps = sp.buf + 2 * static_cast<int64_t>(sp.count++) * sp.max_ctas;
             e = traced(MO_K_GRAM + ph, stream, [&] {
                 return o.precision == MO_NS_BF16 ? launch_ns_tc_phase(np, grids[ph], stream)
                                                  : launch_ns_fp32_phase(np, grids[ph], stream);
@@ -975,9 +974,18 @@ int mo_debug_sm_count(void) {
     return c;
 }
 
-int mo_debug_set_apply_operand(int kmajor) {
-    if (kmajor != 0 && kmajor != 1) return MO_ERR_INVALID_ARG;
-    g_apply_kmajor.store(kmajor);
+int mo_debug_cta_stamps(uint64_t* buf, int capacity, int max_ctas, int* recorded) {
+    Stamps& sp = t_stamps;
+    if (recorded != nullptr) *recorded = sp.count;
+    if (buf == nullptr) {
+        sp = Stamps{};
+        return MO_OK;
+    }
+    if (capacity <= 0 || max_ctas <= 0 || (reinterpret_cast<uintptr_t>(buf) & 7u) != 0) return MO_ERR_INVALID_ARG;
+    sp.buf = reinterpret_cast<unsigned long long*>(buf);
+    sp.capacity = capacity;
+    sp.max_ctas = max_ctas;
+    sp.count = 0;
     return MO_OK;
 }
 

@@ -119,24 +119,21 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) ss = fmaf(x[k], x[k], ss);
-                // the user's own orientation: X itself, or X^T for a transposed matrix
                 if (!md.transposed)
                     store4(md.x_op[0], op_dt, static_cast<int64_t>(r) * md.ldx + c, nvalid, x);
-                else if (p.write_xt)
-                    store4(md.xt_op[0], MO_BF16, static_cast<int64_t>(r) * md.lda + c, nvalid, x);
             }
-            if (md.transposed || p.write_xt) {
+            if (md.transposed) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) tileT[4 * col4 + k][rl] = x[k];
             }
         }
-        if (md.transposed || p.write_xt) {
+        if (md.transposed) {
             __syncthreads();
-            // the other orientation through the tile transpose: row xr = user
-            // column c0 + xr, columns = user rows r0 + seg .. +15
-            void* dst = md.transposed ? md.x_op[0] : md.xt_op[0];
-            const int dt = md.transposed ? op_dt : MO_BF16;
-            const int64_t dld = md.transposed ? md.ldx : md.lda;
+            // through the tile transpose: oriented row xr = user column
+            // c0 + xr, oriented columns = user rows r0 + seg .. +15
+            void* dst = md.x_op[0];
+            const int dt = op_dt;
+            const int64_t dld = md.ldx;
             const int xr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;
             const int orow = c0 + xr;
             if (orow < md.cols) {

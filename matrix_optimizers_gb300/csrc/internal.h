@@ -52,12 +52,10 @@ struct MatDesc {
     void* out;                 // NS output target or null
     uint32_t* sign_words;      // fused sign + 1-bit pack target of the output, or null
     void* x_op[2];             // NS operand ping-pong (bf16 or fp32), m x ldx
-    void* xt_op[2];            // bf16 X^T ping-pong, n x lda (K-major B operand of the apply phase)
     float* x_master;           // fp32 master of X (bf16 mode), m x ldx
     void* gram;                // m x lda  (A = X X^T)
     void* poly;                // m x lda  (B = b A + c A^2)
     const CUtensorMap* tm_x[2];
-    const CUtensorMap* tm_xt[2];
     const CUtensorMap* tm_gram;
     const CUtensorMap* tm_poly;
     float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix)
@@ -85,7 +83,7 @@ struct NsLaunch {
     uint32_t idesc;
     uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
     int32_t ntiles;
-    int32_t b_kmajor;          // apply phase reads X^T (K-major) instead of X (MN-major)
+    unsigned long long* stamps;  // null, or [2 * gridDim.x] CTA start / end %globaltimer (ns)
 };
 
 struct MomLaunch {
@@ -94,7 +92,6 @@ struct MomLaunch {
     int64_t ntiles;
     float mu;
     int32_t fp32_operand;      // write the fp32 operand (fp32 NS) instead of bf16
-    int32_t write_xt;          // also write the bf16 X^T operand
     float* partials;           // one fp32 sum of squares per momentum tile
 };
 

@@ -278,14 +278,6 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
         const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
         store32_stream(md.x_master, off, nv, x);
         store32(md.x_op[(p.step + 1) & 1], MO_BF16, off, nv, x);
-        if (p.b_kmajor) {
-            // X^T for the next apply's K-major B operand: down columns, so
-            // consecutive lanes (rows i) write consecutive addresses
-            bf16* xt = static_cast<bf16*>(md.xt_op[(p.step + 1) & 1]);
-#pragma unroll
-            for (int k = 0; k < 32; ++k)
-                if (k < nv) xt[static_cast<int64_t>(j0 + k) * md.lda + i] = __float2bfloat16_rn(x[k]);
-        }
         return;
     }
     if (md.sign_words != nullptr) {
@@ -336,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
     const int2 range = p.cta_range[blockIdx.x];
-    const bool mn_b = p.phase == kApply && !p.b_kmajor;
+    const bool mn_b = p.phase == kApply;
+    if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[2 * blockIdx.x] = globaltimer_ns();
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -356,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     tma = tmb = md.tm_gram;
                 } else {
                     tma = md.tm_poly;
-                    tmb = p.b_kmajor ? md.tm_xt[p.step & 1] : md.tm_x[p.step & 1];
+                    tmb = md.tm_x[p.step & 1];
                 }
                 for (int kb = 0; kb < td.nkb; ++kb) {
                     const uint32_t empty = smem_u32(&ctl->empty[stage]);
@@ -470,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[2 * blockIdx.x + 1] = globaltimer_ns();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

@@ -82,9 +82,8 @@ def test_workspace_bytes_host_only():
             B.mo_matrix(3072, 768, 768, 0, 0, 0, 0, 16, 16, 16)]
     cfg = B.make_cfg()
     ws = B.mo_workspace_bytes(mats, cfg)
-    # both orient to 768 x 3072: operands 2 x bf16 X + fp32 master + 2 x bf16 X^T
-    # + 2 x 768^2 bf16 each
-    per = 768 * 3072 * (2 + 2 + 4 + 2 + 2) + 2 * 768 * 768 * 2
+    # both orient to 768 x 3072: operands 2 x bf16 X + fp32 master + 2 x 768^2 bf16 each
+    per = 768 * 3072 * (2 + 2 + 4) + 2 * 768 * 768 * 2
     assert 2 * per <= ws < 2 * per + (1 << 20)
     assert ws == B.ns_workspace_bytes([(768, 3072), (3072, 768)])
     cfg32 = B.make_cfg(precision=B.MO_NS_FP32)

@@ -159,7 +159,7 @@ def test_sign_muon_m8_step_bit_exact_vote():
 
 
 @pytest.mark.parametrize("shapes", [[(256, 512), (512, 256)], [(96, 160), (160, 96), (2048, 2048)],
-                                    [(200, 64), (64, 200), (320, 320)]])
+                                    [(200, 64), (64, 224), (320, 320)]])
 def test_sign_packed_step_equals_separate_pack(shapes):
     """Fused sign + pack in the last NS epilogue == sign_pack of the bf16
     direction written by the unfused step, bit for bit."""
