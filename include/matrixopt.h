@@ -75,7 +75,11 @@ typedef struct {
 /* Muon hyper-parameters.  The step is
  *   M <- mu*M + G                          (heavy-ball momentum)
  *   X <- orient(M): M^T when rows > cols   (so m <= n)
- *   X <- X / ||X||_F  (0 stays 0)
+ *   X <- X / ||X||_F  (0 stays 0); with spectral_iters = q > 0 instead
+ *        X <- X / (||X||_F * sigma_hat), sigma_hat^2 = v^T A v after q power
+ *        iterations v <- A v / ||A v|| from v = ones/sqrt(m) on the Gram
+ *        matrix A of X/||X||_F (the spectral scale; SignMuon §4 compares it
+ *        with the Frobenius scale).  bf16 NS and ns_steps >= 1 only.
  *   repeat ns_steps: A = X X^T; B = b*A + c*A*A; X <- a*X + B*X
  *   O <- orient back(X)
  *   apply_update != 0:  W <- W - lr*weight_decay*W - lr*update_scale*O
@@ -87,7 +91,7 @@ typedef struct {
     int32_t ns_precision;          /* MO_NS_BF16 or MO_NS_FP32 */
     int32_t apply_update;
     int32_t out_dtype;             /* MO_F32 / MO_BF16, used when apply_update == 0 */
-    int32_t reserved;
+    int32_t spectral_iters;        /* 0: Frobenius scale; q in 1..64: spectral scale */
 } mo_muon_cfg;
 
 /* The flat float32 tail updated by decoupled AdamW at step number `step`

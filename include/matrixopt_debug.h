@@ -72,6 +72,7 @@ int mo_debug_cta_stamps(uint64_t* buf, int capacity, int max_ctas, int* recorded
 #define MO_K_ADAMW    7
 #define MO_K_PACK     8
 #define MO_K_VOTE     9
+#define MO_K_SPECTRAL 10  /* power-iteration spectral estimate (all of its launches) */
 int mo_trace_enable(int capacity);
 int mo_trace_read(int32_t* kinds, float* ms, int cap, int* count);
 

@@ -41,7 +41,7 @@ class mo_muon_cfg(ctypes.Structure):
                 ("weight_decay", c_float), ("ns_steps", c_int32),
                 ("a", c_float), ("b", c_float), ("c", c_float),
                 ("ns_precision", c_int32), ("apply_update", c_int32),
-                ("out_dtype", c_int32), ("reserved", c_int32)]
+                ("out_dtype", c_int32), ("spectral_iters", c_int32)]
 
 
 class mo_adamw_tail(ctypes.Structure):
@@ -104,7 +104,7 @@ _SIGNATURES = [
 ]
 
 TRACE_KINDS = {1: "momentum_norm", 2: "norm_finalize", 3: "ns_gram", 4: "ns_poly", 5: "ns_apply",
-               6: "ns_k0", 7: "adamw", 8: "sign_pack", 9: "vote_update"}
+               6: "ns_k0", 7: "adamw", 8: "sign_pack", 9: "vote_update", 10: "spectral_estimate"}
 
 _lib = None
 _lock = threading.Lock()
@@ -177,9 +177,9 @@ def make_matrix(W, M, G):
 
 def make_cfg(mu=0.95, lr=0.02, ns_steps=5, a=3.4445, b=-4.7750, c=2.0315,
              precision=MO_NS_BF16, update_scale=1.0, weight_decay=0.0, apply_update=True,
-             out_dtype=MO_BF16):
+             out_dtype=MO_BF16, spectral_iters=0):
     return mo_muon_cfg(mu, lr, update_scale, weight_decay, ns_steps, a, b, c, precision,
-                       1 if apply_update else 0, out_dtype, 0)
+                       1 if apply_update else 0, out_dtype, spectral_iters)
 
 
 def make_tail(W, g, m, v, step, lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0):

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libmatrixopt.so"
-SOURCES = ["api.cu", "elementwise.cu", "ns_tc.cu", "ns_fp32.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "elementwise.cu", "ns_tc.cu", "ns_fp32.cu", "spectral.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

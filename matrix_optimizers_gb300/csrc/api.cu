@@ -128,7 +128,9 @@ int64_t sym_tiles(int64_t m) {
 
 struct Layout {
     int precision;
-    size_t mats, tmaps, tiles[3], ranges[3], partials, scales, bufs_begin, total;
+    size_t mats, tmaps, tiles[3], ranges[3], partials, scales, power, bufs_begin, total;
+    int64_t total_rows;            // sum of m (power-iteration rows)
+    std::vector<size_t> pv;        // per matrix: offset of its two power-iteration vectors
     size_t ctl_bytes;              // [0, ctl_bytes) is uploaded every call
     int64_t ntiles[3];
     int64_t mom_tiles;
@@ -175,7 +177,16 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
     L.partials = off;
     off = align_up(off + static_cast<size_t>(L.mom_tiles) * sizeof(float), 128);
     L.scales = off;
-    off = align_up(off + n * 2 * sizeof(float), kBufAlign);
+    off = align_up(off + n * kScaleStride * sizeof(float), 128);
+    L.power = off;
+    L.pv.resize(n);
+    L.total_rows = 0;
+    for (size_t i = 0; i < n; ++i) {
+        L.pv[i] = off;
+        off = align_up(off + 2 * static_cast<size_t>(L.shape[i].lda) * sizeof(float), 128);
+        L.total_rows += L.shape[i].m;
+    }
+    off = align_up(off, kBufAlign);
     L.bufs_begin = off;
     const size_t xe = precision == MO_NS_BF16 ? 2 : 4;
     for (size_t i = 0; i < n; ++i) {
@@ -259,6 +270,7 @@ int validate_tail(const mo_adamw_tail* t) {
 struct NsOpts {
     int precision, steps, apply_update;
     float mu, a, b, c, alpha, decay;
+    int spectral_iters = 0;        // > 0: spectral-scale normalisation with this many power iterations
 };
 
 // ------------------------------------------------------------ launch trace
@@ -344,12 +356,12 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
     const int nsm = device_sm_count();
     plan->stage.assign(L.ctl_bytes, 0);
     uint8_t* h = plan->stage.data();
-    const NsOpts o{precision, 0, 0, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const NsOpts o{precision, 0, 0, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0};
     MatDesc* hm = reinterpret_cast<MatDesc*>(h + L.mats);
     CUtensorMap* htm = reinterpret_cast<CUtensorMap*>(h + L.tmaps);
     const CUtensorMap* dtm = reinterpret_cast<const CUtensorMap*>(base + L.tmaps);
 
-    int64_t mom_begin = 0;
+    int64_t mom_begin = 0, row_begin = 0;
     for (size_t i = 0; i < jobs.size(); ++i) {
         const Job& j = jobs[i];
         const Shape& s = L.shape[i];
@@ -378,7 +390,11 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
         d.x_master = o.precision == MO_NS_BF16 ? reinterpret_cast<float*>(base + b.x_master) : nullptr;
         d.gram = base + b.gram;
         d.poly = base + b.poly;
-        d.scales = reinterpret_cast<float*>(base + L.scales) + 2 * i;
+        d.scales = reinterpret_cast<float*>(base + L.scales) + kScaleStride * i;
+        d.pv = reinterpret_cast<float*>(base + L.pv[i]);
+        d.py = d.pv + s.lda;
+        d.row_begin = row_begin;
+        row_begin += s.m;
         d.mom_tile_begin = mom_begin;
         d.mom_tiles_r = static_cast<int32_t>(ceil_div(j.rows, kMomTile));
         d.mom_tiles_c = static_cast<int32_t>(ceil_div(j.cols, kMomTile));
@@ -539,6 +555,15 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
                                                  : launch_ns_fp32_phase(np, grids[ph], stream);
             });
             if (e != cudaSuccess) return MO_ERR_CUDA;
+            if (t == 0 && ph == kGram && o.spectral_iters > 0) {
+                // spectral scale: power iteration on the first Gram matrix, folded
+                // into the first polynomial and apply through the per-matrix scales
+                e = traced(MO_K_SPECTRAL, stream, [&] {
+                    return launch_spectral_estimate(dmats, static_cast<int>(jobs.size()), L.total_rows,
+                                                    o.spectral_iters, nsm, stream);
+                });
+                if (e != cudaSuccess) return MO_ERR_CUDA;
+            }
         }
     }
     return MO_OK;
@@ -555,6 +580,9 @@ int gather_muon_jobs(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, void*
     if (n < 0 || cfg == nullptr || (n > 0 && mats == nullptr)) return MO_ERR_INVALID_ARG;
     if (cfg->ns_steps < 0 || (cfg->ns_precision != MO_NS_BF16 && cfg->ns_precision != MO_NS_FP32))
         return MO_ERR_INVALID_ARG;
+    if (cfg->spectral_iters < 0) return MO_ERR_INVALID_ARG;
+    if (cfg->spectral_iters > 0 && (cfg->ns_precision != MO_NS_BF16 || cfg->ns_steps < 1 || cfg->spectral_iters > 64))
+        return MO_ERR_UNSUPPORTED;
     if (!cfg->apply_update && !valid_dtype(cfg->out_dtype)) return MO_ERR_INVALID_ARG;
     if (check_ptrs && !cfg->apply_update && n > 0 && out == nullptr) return MO_ERR_INVALID_ARG;
     jobs.clear();
@@ -652,6 +680,7 @@ int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, cons
     o.c = cfg->c;
     o.alpha = cfg->lr * cfg->update_scale;
     o.decay = cfg->lr * cfg->weight_decay;
+    o.spectral_iters = cfg->spectral_iters;
     return run_ns(jobs, o, ws, ws_bytes, s);
 }
 
@@ -688,6 +717,7 @@ int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, 
     o.c = cfg->c;
     o.alpha = 0.f;
     o.decay = 0.f;
+    o.spectral_iters = cfg->spectral_iters;
     return run_ns(jobs, o, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

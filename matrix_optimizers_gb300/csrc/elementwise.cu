@@ -177,6 +177,9 @@ __global__ void __launch_bounds__(32) norm_finalize_kernel(const MatDesc* mats, 
         }
         md.scales[0] = inv_s;
         md.scales[1] = inv_s2;
+        md.scales[2] = 1.f;     // spectral folding factors: identity under Frobenius scaling
+        md.scales[3] = 1.f;
+        md.scales[4] = 1.f;
     }
 }
 

@@ -58,10 +58,16 @@ struct MatDesc {
     const CUtensorMap* tm_x[2];
     const CUtensorMap* tm_gram;
     const CUtensorMap* tm_poly;
-    float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix)
+    float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix),
+                               // [2..4] = 1/lambda, 1/lambda^2, 1/sqrt(lambda) of the spectral
+                               // estimate (1 under Frobenius scaling); kScaleStride floats
+    float* pv;                 // power-iteration vectors (m floats each)
+    float* py;
+    int64_t row_begin;         // first global row of this matrix (power iteration)
     int64_t mom_tile_begin;    // first global index of this matrix's momentum tiles
     int32_t mom_tiles_r, mom_tiles_c;
 };
+constexpr int kScaleStride = 8;
 
 // One tile of a grouped GEMM phase.
 struct TileDesc {
@@ -111,6 +117,8 @@ cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t
 cudaError_t launch_adamw(const mo_adamw_tail& t, cudaStream_t s);
 cudaError_t launch_sign_pack_batched(const void* const* U, uint32_t* const* words, int M, int dtype, int64_t rows,
                                      int64_t cols, int64_t ld, cudaStream_t s);
+cudaError_t launch_spectral_estimate(const MatDesc* mats, int nmats, int64_t total_rows, int iters, int sm_count,
+                                     cudaStream_t s);
 cudaError_t launch_vote_matrix(const uint32_t* const* words, int M, int64_t rows, int64_t cols, void* S, int64_t ld,
                                cudaStream_t s);
 cudaError_t launch_sign_int8(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld, int8_t* out,

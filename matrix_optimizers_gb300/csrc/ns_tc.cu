@@ -203,8 +203,11 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
     } else {
         float a[32];
         load32(md.gram, MO_BF16, static_cast<int64_t>(i) * md.lda + j0, nv, a);
+        // step 0 folds the spectral scale into the coefficients (1 otherwise)
+        const float bs = p.step == 0 ? p.b * md.scales[2] : p.b;
+        const float cs = p.step == 0 ? p.c * md.scales[3] : p.c;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = fmaf(p.c, v[k], p.b * a[k]);
+        for (int k = 0; k < 32; ++k) v[k] = fmaf(cs, v[k], bs * a[k]);
     }
     const int64_t row = static_cast<int64_t>(i) * md.lda;
     if (j0 >= i) {
@@ -265,7 +268,7 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     float x[32];
     if (p.step == 0) {
         user_load32(md, md.src, md.src_dtype, i, j0, nv, x);
-        const float inv_s = md.scales[0];
+        const float inv_s = md.scales[0] * md.scales[4];      // 1/||M||_F (x 1/sigma_hat when spectral)
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
     } else {

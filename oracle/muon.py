@@ -56,6 +56,36 @@ def frobenius_normalize(X):
     return X / s, s
 
 
+def spectral_estimate(F, iters):
+    """Largest singular value of F by power iteration on the Gram matrix
+    F F^T: v0 = ones/sqrt(m); repeat iters times y = (F F^T) v, v = y/||y||;
+    then sigma^2 = v^T (F F^T) v (the Rayleigh quotient)."""
+    F = np.asarray(F, dtype=np.float64)
+    Gm = F @ F.T
+    m = Gm.shape[0]
+    v = np.ones(m) / np.sqrt(m)
+    for _ in range(iters):
+        y = Gm @ v
+        nrm = np.linalg.norm(y)
+        if nrm == 0.0:
+            return 0.0
+        v = y / nrm
+    lam = float(v @ (Gm @ v))
+    return float(np.sqrt(max(lam, 0.0)))
+
+
+def spectral_normalize(X, iters):
+    """X / sigma_hat: the spectral scale the pages contrast with the
+    Frobenius scale ("Riepilogo Tecnico: SignMuon" §4, nanoGPT).  Reading:
+    sigma_hat is estimated by `iters` power iterations (spectral_estimate) on
+    the Frobenius-normalised matrix, so the result is X/||X||_F/sigma_hat."""
+    F, s = frobenius_normalize(X)
+    if s == 0.0:
+        return F, 0.0
+    sig = spectral_estimate(F, iters)
+    return (F / sig if sig > 0 else np.zeros_like(F)), s * sig
+
+
 def ns_iterate(X0, steps=NS_STEPS, a=NS_A, b=NS_B, c=NS_C):
     """k quintic NS steps on an m x n matrix (any m, n): the pages' local
     orthogonalisation, with the Gram matrix formed on the rows of X."""
@@ -67,11 +97,15 @@ def ns_iterate(X0, steps=NS_STEPS, a=NS_A, b=NS_B, c=NS_C):
     return X
 
 
-def newton_schulz(M, steps=NS_STEPS, a=NS_A, b=NS_B, c=NS_C):
+def newton_schulz(M, steps=NS_STEPS, a=NS_A, b=NS_B, c=NS_C, spectral_iters=0):
     """Orthogonalised direction O of a 2D matrix M, in M's own orientation:
-    orient to m <= n, normalise by the Frobenius norm, iterate, orient back."""
+    orient to m <= n, normalise (Frobenius norm, or the spectral estimate
+    when spectral_iters > 0), iterate, orient back."""
     X, transposed = orient(M)
-    X0, _ = frobenius_normalize(X)
+    if spectral_iters > 0:
+        X0, _ = spectral_normalize(X, spectral_iters)
+    else:
+        X0, _ = frobenius_normalize(X)
     O = ns_iterate(X0, steps, a, b, c)
     return O.T if transposed else O
 
@@ -83,7 +117,7 @@ def muon_update(W, O, lr, update_scale=1.0, weight_decay=0.0):
 
 
 def muon_step(W, M0, G, mu, lr, steps=NS_STEPS, a=NS_A, b=NS_B, c=NS_C,
-              update_scale=1.0, weight_decay=0.0, m_dtype="f32", apply_update=True):
+              update_scale=1.0, weight_decay=0.0, m_dtype="f32", apply_update=True, spectral_iters=0):
     """One Muon step on one matrix.
 
     Returns (W_new, M_stored, O): O is the NS output the update uses.
@@ -94,7 +128,7 @@ def muon_step(W, M0, G, mu, lr, steps=NS_STEPS, a=NS_A, b=NS_B, c=NS_C,
     M1 = momentum(M0, G, mu)
     if m_dtype == "bf16":
         M1 = round_bf16(M1)
-    O = newton_schulz(M1, steps, a, b, c)
+    O = newton_schulz(M1, steps, a, b, c, spectral_iters)
     W_new = muon_update(W, O, lr, update_scale, weight_decay) if apply_update \
         else np.asarray(W, dtype=np.float64)
     return W_new, M1, O

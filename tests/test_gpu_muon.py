@@ -200,6 +200,22 @@ def test_sign_packed_step_rejects_unaligned_columns():
     assert e.value.status == -6
 
 
+@pytest.mark.parametrize("shapes", [[(256, 512)], [(512, 256), (768, 3072), (96, 200)]])
+def test_spectral_scale_vs_oracle(shapes):
+    rng = np.random.default_rng(31 + len(shapes))
+    inputs = [{"W": (0.02 * rng.standard_normal(s)).astype(np.float32),
+               "G": rng.standard_normal(s).astype(np.float32)} for s in shapes]
+    cfg = mo.make_cfg(mu=0.95, lr=0.02, spectral_iters=8)
+    Ws, _ = _run(inputs, cfg)
+    for w, inp in zip(Ws, inputs):
+        W0 = inp["W"].astype(np.float64)
+        Wn, _, _ = om.muon_step(W0, np.zeros_like(W0), inp["G"], mu=0.95, lr=0.02, spectral_iters=8)
+        Wf, _, _ = om.muon_step(W0, np.zeros_like(W0), inp["G"], mu=0.95, lr=0.02)
+        d = to_np(w) - W0
+        assert rel_fro(d, Wn - W0) < NS_BF16_TOL
+        assert rel_fro(d, Wf - W0) > 5 * NS_BF16_TOL           # the spectral path is really taken
+
+
 @pytest.mark.slow
 def test_llama7b_owner0_sampled():
     c = CONFIGS["llama7b_owner0"]

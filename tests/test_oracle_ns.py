@@ -152,6 +152,34 @@ def test_ns_degenerate_cases():
     assert np.array_equal(om.newton_schulz(Z), Z)
 
 
+def test_spectral_estimate_converges_to_sigma_max():
+    rng = np.random.default_rng(14)
+    Q1, _ = np.linalg.qr(rng.standard_normal((16, 16)))
+    Q2, _ = np.linalg.qr(rng.standard_normal((30, 30)))
+    s = np.array([3.0] + list(np.linspace(0.2, 1.5, 15)))    # a clear spectral gap
+    M = (Q1 * s) @ Q2[:16]
+    assert abs(om.spectral_estimate(M, 60) - 3.0) < 1e-10
+    # power iteration from below: each iterate's Rayleigh quotient is <= sigma_max^2
+    assert all(om.spectral_estimate(M, q) <= 3.0 + 1e-12 for q in range(0, 8))
+    X0, scale = om.spectral_normalize(M, 60)
+    np.testing.assert_allclose(X0, M / 3.0, atol=1e-12)
+    assert abs(scale - 3.0) < 1e-10
+
+
+def test_spectral_scaled_ns_closed_form_and_invariance():
+    rng = np.random.default_rng(15)
+    M = rng.standard_normal((20, 36))
+    O = om.newton_schulz(M, 5, spectral_iters=8)
+    F = M / np.linalg.norm(M)
+    sig = om.spectral_estimate(F, 8)
+    U, S, Vt = np.linalg.svd(F / sig, full_matrices=False)
+    for _ in range(5):
+        S = _p(S)
+    np.testing.assert_allclose(O, (U * S) @ Vt, atol=1e-11)
+    np.testing.assert_allclose(om.newton_schulz(2.5 * M, 5, spectral_iters=8), O, atol=1e-12)
+    np.testing.assert_allclose(om.newton_schulz(M.T, 5, spectral_iters=8), O.T, atol=1e-12)
+
+
 def test_momentum_special_cases():
     rng = np.random.default_rng(12)
     M0, G = rng.standard_normal((5, 7)), rng.standard_normal((5, 7))
