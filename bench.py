@@ -200,12 +200,27 @@ def run_gb300(args, rank, world, local_rank, dist):
     if args.max_matrices:
         idx = idx[: args.max_matrices]
     shapes = [shapes_all[i] for i in idx]
-    inputs = matrix_set_inputs(shapes_all, idx)
-    Ws = [torch.from_numpy(x["W"]).to(dev) for x in inputs]
-    Gs = [torch.from_numpy(x["G"]).to(dev) for x in inputs]
-    Ms = [torch.zeros(s, dtype=torch.float32, device=dev) for s in shapes]
-    mats = [mo.make_matrix(w, m, g) for w, m, g in zip(Ws, Ms, Gs)]
-    cfg = mo.make_cfg(mu=cfgd["mu"], lr=cfgd["lr"])
+    sign_muon = args.workload == "sign_muon_m8"
+    if sign_muon:
+        # Sign-Muon: 8 workers' gradients (shared N(0,1) + per-worker noise),
+        # bf16 momentum, one shared float32 W updated by the vote
+        from workloads import sign_muon_inputs
+        sm_in = sign_muon_inputs()
+        inputs = [{"G": g} for g in sm_in["G"]]
+        Gs = [torch.from_numpy(g).to(dev) for g in sm_in["G"]]
+        Ms = [torch.zeros(s, dtype=torch.bfloat16, device=dev) for s in shapes]
+        Wv = torch.from_numpy(sm_in["W"]).to(dev)
+        Ws = [Wv]
+        words = [torch.empty((s[0] * s[1] + 31) // 32, dtype=torch.int32, device=dev) for s in shapes]
+        mats = [mo.make_matrix(m, m, g) for m, g in zip(Ms, Gs)]
+        cfg = mo.make_cfg(mu=cfgd["mu"], lr=cfgd["lr"], apply_update=False, out_dtype=mo.MO_BF16)
+    else:
+        inputs = matrix_set_inputs(shapes_all, idx)
+        Ws = [torch.from_numpy(x["W"]).to(dev) for x in inputs]
+        Gs = [torch.from_numpy(x["G"]).to(dev) for x in inputs]
+        Ms = [torch.zeros(s, dtype=torch.float32, device=dev) for s in shapes]
+        mats = [mo.make_matrix(w, m, g) for w, m, g in zip(Ws, Ms, Gs)]
+        cfg = mo.make_cfg(mu=cfgd["mu"], lr=cfgd["lr"])
     ws = torch.empty(mo.mo_workspace_bytes(mats, cfg), dtype=torch.uint8, device=dev)
     tail = None
     tail_bytes = 0
@@ -214,11 +229,15 @@ def run_gb300(args, rank, world, local_rank, dist):
         tt = {k: torch.from_numpy(t[k]).to(dev) for k in ("W", "g", "m", "v")}
         tail = mo.make_tail(tt["W"], tt["g"], tt["m"], tt["v"], step=1, lr=cfgd["tail_lr"])
         tail_bytes = 28 * cfgd["tail_numel"]
-    resident = sum(x.numel() * 4 * 3 for x in Ws) + ws.numel()
+    resident = sum(g.numel() * 4 * 3 for g in Gs) + ws.numel()
     stream = torch.cuda.current_stream()
 
     def step():
-        mo.muon_step_batched(mats, cfg, ws, tail=tail)
+        if sign_muon:
+            mo.muon_step_sign_packed(mats, cfg, words, ws)
+            mo.sign_vote_update(words, Wv, cfgd["lr"])
+        else:
+            mo.muon_step_batched(mats, cfg, ws, tail=tail)
 
     for _ in range(args.warmup):
         step()
@@ -271,7 +290,9 @@ def run_gb300(args, rank, world, local_rank, dist):
         "metric": METRIC, "value": total_mats / (ms_step * 1e-3), "unit": "matrices/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic: seeded N(0,0.02^2) weights, N(0,1e-3^2) gradients, zero initial momentum",
+        "data": ("synthetic: 8 workers' gradients N(0,1) shared + N(0,0.5^2) per worker, bf16 momentum from 0, "
+                 "N(0,0.02^2) shared W; step = fused sign-packed NS per worker + majority-vote update")
+        if sign_muon else "synthetic: seeded N(0,0.02^2) weights, N(0,1e-3^2) gradients, zero initial momentum",
         "config": {
             "workload": args.workload, "matrices_per_gpu": len(shapes),
             "shapes": _shape_summary(shapes), "ns_steps": 5, "ns_coeffs": [3.4445, -4.7750, 2.0315],
@@ -300,7 +321,8 @@ def run_gb300(args, rank, world, local_rank, dist):
     }
     if "momentum_norm" in by_kind:
         mom = by_kind["momentum_norm"]
-        gbs = sum(r * c for r, c in shapes) * 14 / (mom[1] / mom[0] * 1e-3) / 1e9
+        per_elt = 10 if sign_muon else 14          # bf16 momentum: M 2+2, G 4, operand 2
+        gbs = sum(r * c for r, c in shapes) * per_elt / (mom[1] / mom[0] * 1e-3) / 1e9
         result["momentum_norm_gbs"] = gbs
         result["momentum_norm_frac_of_hbm"] = gbs / peaks["hbm_gbs"]
     if tail is not None and "adamw" in by_kind:
@@ -311,7 +333,7 @@ def run_gb300(args, rank, world, local_rank, dist):
     # ---------------- e2e: pinned host G in and W out inside the timed region
     if not args.no_e2e:
         hG = [torch.from_numpy(x["G"]).pin_memory() for x in inputs]
-        hW = [torch.empty(s, dtype=torch.float32).pin_memory() for s in shapes]
+        hW = [torch.empty(w.shape, dtype=torch.float32).pin_memory() for w in Ws]
         h2d = sum(g.numel() * 4 for g in hG)
         d2h = sum(w.numel() * 4 for w in hW)
 
