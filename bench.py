@@ -154,7 +154,12 @@ def _sm_balance(st):
     phases = {}
     for k, r in enumerate(ratios):
         phases.setdefault(("gram", "poly", "apply")[k % 3], []).append(r)
-    return {"launches": len(ratios), "ctas_per_launch_max": int(st.shape[1]),
+    waits = {}
+    if st.shape[2] >= 4 and st[:, :, 3].sum() > 0:
+        busy_all = np.where(st[:, :, 1] > 0, st[:, :, 1] - st[:, :, 0], 0).astype(np.float64)
+        waits = {"dep_wait_frac_of_busy": float(st[:, :, 2].sum() / max(1.0, busy_all.sum())),
+                 "dep_spinning_waits_per_cta_launch": float(st[:, :, 3].mean())}
+    return {"launches": len(ratios), "ctas_per_launch_max": int(st.shape[1]), **waits,
             "max_over_mean_busy": sum_max / sum_mean,
             "per_launch_median": float(np.median(ratios)), "per_launch_worst": float(np.max(ratios)),
             "per_phase_median": {k: float(np.median(v)) for k, v in phases.items()},
@@ -232,6 +237,9 @@ def run_gb300(args, rank, world, local_rank, dist):
     resident = sum(g.numel() * 4 * 3 for g in Gs) + ws.numel()
     stream = torch.cuda.current_stream()
 
+    from matrix_optimizers_gb300 import _binding
+    _binding.mo_debug_set_ns_fused({"phases": 0, "fused-matrix": 1, "fused-level": 2, "fused": 3}[args.ns_launch])
+
     def step():
         if sign_muon:
             mo.muon_step_sign_packed(mats, cfg, words, ws)
@@ -245,10 +253,9 @@ def run_gb300(args, rank, world, local_rank, dist):
     if mo.mo_check_device_status(ws) != 0:
         raise SystemExit("device status error after warm-up")
 
-    from matrix_optimizers_gb300 import _binding
     n_ns = 3 * 5 * args.steps
     max_ctas = torch.cuda.get_device_properties(dev).multi_processor_count
-    stamps = torch.zeros(2 * n_ns * max_ctas, dtype=torch.int64, device=dev)
+    stamps = torch.zeros(4 * n_ns * max_ctas, dtype=torch.int64, device=dev)
     _binding.mo_debug_cta_stamps(stamps, n_ns, max_ctas)
     mo.mo_trace_enable(64 * (args.steps + 1))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -266,7 +273,7 @@ def run_gb300(args, rank, world, local_rank, dist):
     trace = mo.mo_trace_read()
     mo.mo_trace_enable(0)
     recorded = _binding.mo_debug_cta_stamps(None, 0, 0)
-    sm_balance = _sm_balance(stamps.view(n_ns, max_ctas, 2).cpu().numpy()[:recorded])
+    sm_balance = _sm_balance(stamps.view(n_ns, max_ctas, 4).cpu().numpy()[:recorded])
     status = mo.mo_check_device_status(ws)
     ms_step = _max_over_ranks(e0.elapsed_time(e1) / args.steps, dist)
     total_mats = _sum_over_ranks(float(len(shapes)), dist)
@@ -277,7 +284,7 @@ def run_gb300(args, rank, world, local_rank, dist):
         d = by_kind.setdefault(k, [0, 0.0])
         d[0] += 1
         d[1] += ms
-    ns_kinds = ("ns_gram", "ns_poly", "ns_apply")
+    ns_kinds = ("ns_gram", "ns_poly", "ns_apply", "ns_fused", "spectral_estimate")
     ns_ms = sum(by_kind[k][1] for k in ns_kinds if k in by_kind)
     ns_launches = sum(by_kind[k][0] for k in ns_kinds if k in by_kind)
     flops_step = sum(ns_flops(s) for s in shapes)
@@ -300,13 +307,15 @@ def run_gb300(args, rank, world, local_rank, dist):
             "l2": f"inputs larger than L2: {resident / 1e9:.1f} GB resident per GPU, no flush",
             "parallelism": f"owner-sharded: each GPU steps one share of a {max(8, world)}-rank owner plan",
             "precision": "bf16 tensor-core operands, fp32 accumulate / master / momentum",
+            "ns_launch": args.ns_launch,
         },
         "ns_tflops": ns_tflops_step,
         "ns_frac_of_bf16_peak": ns_tflops_step / sustained,
         "ns_tflops_kernels_only": ns_tflops_kernel,
         "ns_issued_tflops_kernels_only": (issued_step * args.steps / (ns_ms * 1e-3) / 1e12) if ns_ms else None,
         "roofline": {
-            "kernel": "ns_tc_kernel (Gram / polynomial / apply phases)",
+            "kernel": ("ns_tc_kernel, one launch per Gram / polynomial / apply phase" if args.ns_launch == "phases"
+                       else "ns_tc_kernel, one fused launch of all Gram / polynomial / apply levels per step"),
             "bound": "tensor", "achieved": ns_tflops_kernel, "peak": sustained, "unit": "TFLOP/s",
             "frac": (ns_tflops_kernel / sustained) if ns_tflops_kernel else None,
             "peak_source": f"{peaks['source']} bf16 sustained (the kernel runs inside a long step)",
@@ -532,6 +541,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="llama7b_owner0")
+    ap.add_argument("--ns-launch", default="fused", choices=["fused", "fused-matrix", "fused-level", "phases"],
+                    help="NS iterations as one fused cooperative launch per step ordered by per-matrix "
+                         "(fused-matrix) or grid-wide (fused-level) counters, or the library's choice "
+                         "between them by size (fused), or one launch per phase")
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -25,11 +25,18 @@ extern "C" {
  *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong (x_master = 0),
  *              gram, poly = fp32 m x m.
  * After a call with steps = 1 the gram buffer holds X0 X0^T and the poly
- * buffer b*A + c*A*A of that step. */
+ * buffer b*A + c*A*A of that step.
+ * deps: three int32 completion counters (Gram, polynomial, apply) of a fused
+ * bf16 launch; after a fused call each holds 16 x (that phase's tiles of this
+ * matrix: tiles_sym for Gram and polynomial, tiles_apply for apply) x (the
+ * steps of that phase the fused launch ran); all three stay 0 after a call
+ * with one launch per phase. */
 typedef struct {
     int64_t m, n, ldx, lda;
     int32_t transposed, precision;
     int64_t x_op[2], x_master, gram, poly;
+    int64_t deps;
+    int32_t tiles_sym, tiles_apply;
 } mo_ns_view;
 
 int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precision,
@@ -46,11 +53,28 @@ int mo_debug_sm_count(void);
  * affects launches issued after the call. */
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
+/* Chooses how the bf16 tensor-core Newton-Schulz iterations are launched:
+ *   1: every (step, phase) of a call in one cooperative persistent launch,
+ *      each tile waiting on per-matrix completion counters for the tiles
+ *      whose results it reads or whose inputs it overwrites;
+ *   2: the same launch with one grid-wide counter set, so each phase waits
+ *      for the whole previous phase of every matrix;
+ *   3 (the default): 1 when a symmetric phase has fewer than 16 tiles per
+ *      CTA, else 2;
+ *   0: one launch per (step, phase).
+ * The fused modes fall back to 0 when the grid cannot be co-resident.  All
+ * modes compute identical results.  Returns the previous setting, or
+ * MO_ERR_INVALID_ARG for a value outside 0..3.  Process-wide; affects calls
+ * issued after it. */
+int mo_debug_set_ns_fused(int on);
+
 /* SM load-balance record.  With a device buffer `buf` of
- * 2 * capacity * max_ctas uint64 values, each of the calling thread's next
+ * 4 * capacity * max_ctas uint64 values, each of the calling thread's next
  * `capacity` tensor-core Newton-Schulz launches (grid <= max_ctas) has CTA c
- * write its start and end %globaltimer (ns) to buf[2*(k*max_ctas + c)] and
- * [.. + 1], k counting launches from 0.  *recorded (nullable) receives the
+ * write, at buf[4*(k*max_ctas + c)] onwards (k counting launches from 0):
+ * its start and end %globaltimer (ns), the ns its TMA producer spent waiting
+ * on fused-launch dependencies, and the number of those waits that had to
+ * spin (both 0 for a per-phase launch).  *recorded (nullable) receives the
  * number of launches recorded since the previous call.  buf = NULL stops
  * recording.  Measurement only: no effect on results. */
 int mo_debug_cta_stamps(uint64_t* buf, int capacity, int max_ctas, int* recorded);
@@ -73,6 +97,7 @@ int mo_debug_cta_stamps(uint64_t* buf, int capacity, int max_ctas, int* recorded
 #define MO_K_PACK     8
 #define MO_K_VOTE     9
 #define MO_K_SPECTRAL 10  /* power-iteration spectral estimate (all of its launches) */
+#define MO_K_NS_FUSED 11  /* all NS levels of a call in one launch (Gram, polynomial, apply) */
 int mo_trace_enable(int capacity);
 int mo_trace_read(int32_t* kinds, float* ms, int cap, int* count);
 

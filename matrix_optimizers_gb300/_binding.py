@@ -55,7 +55,7 @@ class mo_ns_view(ctypes.Structure):
     _fields_ = [("m", c_int64), ("n", c_int64), ("ldx", c_int64), ("lda", c_int64),
                 ("transposed", c_int32), ("precision", c_int32),
                 ("x_op", c_int64 * 2), ("x_master", c_int64), ("gram", c_int64),
-                ("poly", c_int64)]
+                ("poly", c_int64), ("deps", c_int64), ("tiles_sym", c_int32), ("tiles_apply", c_int32)]
 
 
 # (name, restype, argtypes) of every exported symbol declared in include/*.h
@@ -97,6 +97,7 @@ _SIGNATURES = [
                                    c_int32, ctypes.POINTER(mo_ns_view)]),
     ("mo_debug_sm_count", c_int32, []),
     ("mo_debug_set_mn_strides", c_int32, [ctypes.c_uint32, ctypes.c_uint32]),
+    ("mo_debug_set_ns_fused", c_int32, [c_int32]),
     ("mo_debug_cta_stamps", c_int32, [c_void_p, c_int32, c_int32, ctypes.POINTER(c_int32)]),
     ("mo_trace_enable", c_int32, [c_int32]),
     ("mo_trace_read", c_int32, [ctypes.POINTER(c_int32), ctypes.POINTER(c_float), c_int32,
@@ -104,7 +105,8 @@ _SIGNATURES = [
 ]
 
 TRACE_KINDS = {1: "momentum_norm", 2: "norm_finalize", 3: "ns_gram", 4: "ns_poly", 5: "ns_apply",
-               6: "ns_k0", 7: "adamw", 8: "sign_pack", 9: "vote_update", 10: "spectral_estimate"}
+               6: "ns_k0", 7: "adamw", 8: "sign_pack", 9: "vote_update", 10: "spectral_estimate",
+               11: "ns_fused"}
 
 _lib = None
 _lock = threading.Lock()
@@ -350,10 +352,20 @@ def mo_debug_set_mn_strides(lbo, sbo):
     _check(load().mo_debug_set_mn_strides(lbo, sbo))
 
 
+def mo_debug_set_ns_fused(on):
+    """Selects the NS launch schedule: 1 / True fused with per-matrix
+    counters, 2 fused with grid-wide counters, 3 (default) either by size,
+    0 / False one launch per phase; returns the previous setting."""
+    prev = load().mo_debug_set_ns_fused(int(on))
+    _check(prev if prev < 0 else 0)
+    return prev
+
+
 def mo_debug_cta_stamps(buf, capacity, max_ctas):
-    """Start recording per-CTA start/end stamps into ``buf`` (int64 CUDA
-    tensor of 2*capacity*max_ctas entries); ``buf=None`` stops.  Returns the
-    number of launches recorded since the previous call."""
+    """Start recording per-CTA stamps (start, end, dependency-wait ns,
+    spinning waits) into ``buf`` (int64 CUDA tensor of 4*capacity*max_ctas
+    entries); ``buf=None`` stops.  Returns the number of launches recorded
+    since the previous call."""
     rec = c_int32(0)
     _check(load().mo_debug_cta_stamps(_ptr(buf), capacity, max_ctas, ctypes.byref(rec)))
     return rec.value

@@ -84,6 +84,16 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 // 8-row K groups of 1 KB).  Exposed to tests through the debug header.
 std::atomic<uint32_t> g_mn_lbo{8192};
 std::atomic<uint32_t> g_mn_sbo{1024};
+// How the tensor-core iterations are launched: 1 one fused cooperative launch
+// (when the grid fits on the device at once) ordered by per-matrix counters;
+// 2 the same launch ordered by one grid-wide counter set; 3 (default) 1 when a
+// symmetric level holds few tiles per CTA, else 2; 0 one launch per (step, phase).
+std::atomic<int> g_ns_fused{3};
+// Below this many symmetric-phase tiles per CTA the barrier tail of each level
+// is a large share of it, and per-matrix ordering (which lets one matrix's
+// next phase fill the tail) wins; above it the grid-wide ordering keeps every
+// CTA on the same few matrices, which measured faster through L2 reuse.
+constexpr int64_t kPerMatrixDepsMaxSymTilesPerCta = 16;
 
 // ------------------------------------------------------------- the request
 struct Job {
@@ -128,7 +138,7 @@ int64_t sym_tiles(int64_t m) {
 
 struct Layout {
     int precision;
-    size_t mats, tmaps, tiles[3], ranges[3], partials, scales, power, bufs_begin, total;
+    size_t mats, tmaps, tiles[3], ranges[3], deps, partials, scales, power, bufs_begin, total;
     int64_t total_rows;            // sum of m (power-iteration rows)
     std::vector<size_t> pv;        // per matrix: offset of its two power-iteration vectors
     size_t ctl_bytes;              // [0, ctl_bytes) is uploaded every call
@@ -173,6 +183,8 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
         L.ranges[ph] = off;
         off = align_up(off + static_cast<size_t>(L.ntiles[ph]) * sizeof(int2), 128);
     }
+    L.deps = off;                  // per matrix 4 ints (3 used), then the grid-wide set; zeroed by every upload
+    off = align_up(off + (n + 1) * 4 * sizeof(int), 128);
     L.ctl_bytes = off;
     L.partials = off;
     off = align_up(off + static_cast<size_t>(L.mom_tiles) * sizeof(float), 128);
@@ -284,9 +296,8 @@ struct Trace {
 };
 thread_local Trace t_trace;
 
-// Optional per-CTA start / end stamps of the tensor-core NS launches
-// (mo_debug_cta_stamps): launch k of the record writes 2 * max_ctas values
-// at buf + 2 * k * max_ctas.
+// Optional per-CTA stamps of the tensor-core NS launches (mo_debug_cta_stamps):
+// launch k of the record writes 4 * max_ctas values at buf + 4 * k * max_ctas.
 struct Stamps {
     unsigned long long* buf = nullptr;
     int capacity = 0, max_ctas = 0, count = 0;
@@ -399,6 +410,9 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
         d.mom_tiles_r = static_cast<int32_t>(ceil_div(j.rows, kMomTile));
         d.mom_tiles_c = static_cast<int32_t>(ceil_div(j.cols, kMomTile));
         mom_begin += static_cast<int64_t>(d.mom_tiles_r) * d.mom_tiles_c;
+        d.nt_sym = static_cast<int32_t>(sym_tiles(s.m));
+        d.nt_apply = static_cast<int32_t>(ceil_div(s.m, kTcBM) * ceil_div(s.n, kTcBN));
+        d.deps = reinterpret_cast<int*>(base + L.deps) + 4 * i;
         if (o.precision == MO_NS_BF16) {
             for (int q = 0; q < 2; ++q) {
                 if (!encode_bf16_map(&htm[4 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
@@ -526,7 +540,7 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
                    [&] { return launch_ns_k0(mp, o.alpha, o.decay, o.apply_update, mom_grid, stream); });
         return map_cuda(e);
     }
-    NsLaunch np;
+    NsLaunch np{};
     np.mats = dmats;
     np.err = reinterpret_cast<int*>(base);
     np.steps = o.steps;
@@ -538,33 +552,59 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     np.decay = o.decay;
     np.mn_lbo = g_mn_lbo.load();
     np.mn_sbo = g_mn_sbo.load();
-    for (int t = 0; t < o.steps; ++t) {
-        for (int ph = 0; ph < 3; ++ph) {
-            np.phase = ph;
-            np.step = t;
-            np.tiles = reinterpret_cast<const TileDesc*>(base + L.tiles[ph]);
-            np.cta_range = reinterpret_cast<const int2*>(base + L.ranges[ph]);
-            np.ntiles = static_cast<int32_t>(L.ntiles[ph]);
-            np.idesc = idesc_bf16_f32(kTcBM, kTcBN, ph == kApply ? 1u : 0u);
-            np.stamps = nullptr;
-            Stamps& sp = t_stamps;
-            if (o.precision == MO_NS_BF16 && sp.buf != nullptr && sp.count < sp.capacity && grids[ph] <= sp.max_ctas)
-                np.stamps = sp.buf + 2 * static_cast<int64_t>(sp.count++) * sp.max_ctas;
-            e = traced(MO_K_GRAM + ph, stream, [&] {
-                return o.precision == MO_NS_BF16 ? launch_ns_tc_phase(np, grids[ph], stream)
-                                                 : launch_ns_fp32_phase(np, grids[ph], stream);
+    np.level_deps = reinterpret_cast<int*>(base + L.deps) + 4 * jobs.size();
+    np.tot_sym = static_cast<int32_t>(L.ntiles[kGram]);
+    np.tot_apply = static_cast<int32_t>(L.ntiles[kApply]);
+    np.idesc_sym = idesc_bf16_f32(kTcBM, kTcBN, 0u);
+    np.idesc_apply = idesc_bf16_f32(kTcBM, kTcBN, 1u);
+    for (int ph = 0; ph < 3; ++ph) {
+        np.tc_tiles[ph] = reinterpret_cast<const TileDesc*>(base + L.tiles[ph]);
+        np.tc_ranges[ph] = reinterpret_cast<const int2*>(base + L.ranges[ph]);
+        np.tc_ctas[ph] = grids[ph];
+    }
+    const bool tc = o.precision == MO_NS_BF16;
+    const int levels = 3 * o.steps;
+    const int grid_fused = std::max(grids[0], std::max(grids[1], grids[2]));
+    int mode = g_ns_fused.load();             // 0 per-phase, 1 / 2 fused (counter granularity)
+    if (mode == 3) mode = L.ntiles[kGram] < kPerMatrixDepsMaxSymTilesPerCta * grid_fused ? 1 : 2;
+
+    // one launch of levels [lv0, lv1): the per-phase form, or the fused one
+    auto launch_levels = [&](int lv0, int lv1) -> cudaError_t {
+        const bool fused = lv1 - lv0 > 1;
+        np.lv_begin = lv0;
+        np.lv_end = lv1;
+        np.deps = fused ? mode : 0;
+        np.phase = lv0 % 3;
+        np.step = lv0 / 3;
+        np.tiles = reinterpret_cast<const TileDesc*>(base + L.tiles[np.phase]);
+        np.ntiles = static_cast<int32_t>(L.ntiles[np.phase]);
+        const int grid = fused ? grid_fused : grids[np.phase];
+        np.stamps = nullptr;
+        Stamps& sp = t_stamps;
+        if (tc && sp.buf != nullptr && sp.count < sp.capacity && grid <= sp.max_ctas)
+            np.stamps = sp.buf + 4 * static_cast<int64_t>(sp.count++) * sp.max_ctas;
+        return traced(fused ? MO_K_NS_FUSED : MO_K_GRAM + np.phase, stream, [&] {
+            return tc ? launch_ns_tc(np, grid, fused, stream) : launch_ns_fp32_phase(np, grid, stream);
+        });
+    };
+
+    // the spectral estimate runs between the first Gram phase and the rest
+    const int lv_fuse = o.spectral_iters > 0 ? 1 : 0;
+    const bool fuse = tc && mode != 0 && levels - lv_fuse > 1 &&
+                      grid_fused <= tc_max_coresident_ctas();
+    for (int lv = 0; lv < levels;) {
+        const int lv1 = fuse && lv >= lv_fuse ? levels : lv + 1;
+        if ((e = launch_levels(lv, lv1)) != cudaSuccess) return MO_ERR_CUDA;
+        if (lv == 0 && o.spectral_iters > 0) {
+            // spectral scale: power iteration on the first Gram matrix, folded
+            // into the first polynomial and apply through the per-matrix scales
+            e = traced(MO_K_SPECTRAL, stream, [&] {
+                return launch_spectral_estimate(dmats, static_cast<int>(jobs.size()), L.total_rows,
+                                                o.spectral_iters, nsm, stream);
             });
             if (e != cudaSuccess) return MO_ERR_CUDA;
-            if (t == 0 && ph == kGram && o.spectral_iters > 0) {
-                // spectral scale: power iteration on the first Gram matrix, folded
-                // into the first polynomial and apply through the per-matrix scales
-                e = traced(MO_K_SPECTRAL, stream, [&] {
-                    return launch_spectral_estimate(dmats, static_cast<int>(jobs.size()), L.total_rows,
-                                                    o.spectral_iters, nsm, stream);
-                });
-                if (e != cudaSuccess) return MO_ERR_CUDA;
-            }
         }
+        lv = lv1;
     }
     return MO_OK;
 }
@@ -993,6 +1033,9 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
     view->x_master = static_cast<int64_t>(b.x_master);
     view->gram = static_cast<int64_t>(b.gram);
     view->poly = static_cast<int64_t>(b.poly);
+    view->deps = static_cast<int64_t>(L.deps + 4 * sizeof(int) * static_cast<size_t>(active));
+    view->tiles_sym = static_cast<int32_t>(sym_tiles(s.m));
+    view->tiles_apply = static_cast<int32_t>(ceil_div(s.m, kTcBM) * ceil_div(s.n, kTcBN));
     return MO_OK;
 }
 
@@ -1047,6 +1090,11 @@ int mo_trace_read(int32_t* kinds, float* ms, int cap, int* count) {
     *count = t.count;
     t.count = 0;
     return MO_OK;
+}
+
+int mo_debug_set_ns_fused(int on) {
+    if (on < 0 || on > 3) return MO_ERR_INVALID_ARG;
+    return g_ns_fused.exchange(on);
 }
 
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo) {

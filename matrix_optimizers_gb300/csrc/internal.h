@@ -66,6 +66,8 @@ struct MatDesc {
     int64_t row_begin;         // first global row of this matrix (power iteration)
     int64_t mom_tile_begin;    // first global index of this matrix's momentum tiles
     int32_t mom_tiles_r, mom_tiles_c;
+    int32_t nt_sym, nt_apply;  // tensor-core tiles of one Gram / polynomial phase, of one apply phase
+    int* deps;                 // [3] epilogue-warp tile completions per phase within one fused launch
 };
 constexpr int kScaleStride = 8;
 
@@ -78,18 +80,28 @@ struct TileDesc {
 
 struct NsLaunch {
     const MatDesc* mats;
-    const TileDesc* tiles;
-    const int2* cta_range;     // per CTA {first tile, tile count} (tensor-core path)
+    const TileDesc* tiles;     // CUDA-core path: one tile per block of phase `phase`
     int* err;
     int32_t phase, step, steps;
     int32_t apply_update;
     float a, b, c;
     float alpha;               // lr * update_scale
     float decay;               // lr * weight_decay
-    uint32_t idesc;
-    uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
     int32_t ntiles;
-    unsigned long long* stamps;  // null, or [2 * gridDim.x] CTA start / end %globaltimer (ns)
+    // tensor-core path: the launch runs levels [lv_begin, lv_end), level = 3 * step + phase,
+    // each CTA walking its scheduled tiles of every level in order
+    const TileDesc* tc_tiles[3];
+    const int2* tc_ranges[3];  // per CTA {first tile, tile count} of each phase
+    int32_t tc_ctas[3];        // CTAs that hold tiles of each phase
+    int32_t lv_begin, lv_end;
+    int32_t deps;              // 0: none (one level); 1: per-matrix counters; 2: one grid-wide
+                               // counter set (every tile of a level waits for the whole previous level)
+    int* level_deps;           // [3] the grid-wide counters of mode 2
+    int32_t tot_sym, tot_apply;  // tiles of one symmetric / apply level over all matrices
+    uint32_t idesc_sym, idesc_apply;
+    uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
+    unsigned long long* stamps;  // null, or [4 * gridDim.x]: per CTA start / end %globaltimer (ns),
+                                 // ns spent waiting on dependencies, number of waits that spun
 };
 
 struct MomLaunch {
@@ -107,7 +119,8 @@ cudaError_t launch_norm_finalize(const MatDesc* mats, int nmats, const float* pa
                                  cudaStream_t s);
 cudaError_t launch_ns_k0(const MomLaunch& p, float alpha, float decay, int apply_update, int grid,
                          cudaStream_t s);
-cudaError_t launch_ns_tc_phase(const NsLaunch& p, int grid, cudaStream_t s);
+cudaError_t launch_ns_tc(const NsLaunch& p, int grid, bool cooperative, cudaStream_t s);
+int tc_max_coresident_ctas();   // CTAs of the tensor-core kernel that fit on the device at once
 cudaError_t launch_ns_fp32_phase(const NsLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
                              uint32_t* words, cudaStream_t s);

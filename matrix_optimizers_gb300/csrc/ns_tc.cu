@@ -1,12 +1,19 @@
 // Grouped tensor-core GEMM for the quintic Newton-Schulz step on sm_103a.
 //
-// One persistent launch per phase covers every matrix of the batch:
+// Three phases per iteration, each a grouped GEMM over every matrix of the batch:
 //   kGram   A = s * X X^T          (X: m x n bf16, K = n; s = 1/||M||_F^2 at step 0)
 //   kPoly   B = b*A + c * A A      (K = m; A is symmetric so A A = A A^T)
 //   kApply  X' = a*X + B X         (K = m; step 0: X' = (a*M + B Xb)/||M||_F)
 //           the last step writes W <- W - lr*wd*W - lr*scale*X' (or the output)
 // kGram and kPoly compute only the 128 x 256 tiles that meet the upper
 // triangle (j >= i) and store each upper element at (i, j) and (j, i).
+//
+// A launch runs a range of (step, phase) levels.  With one level per launch
+// the kernel boundary orders the phases.  A fused launch runs all levels in
+// one cooperative persistent grid: each CTA walks its scheduled tiles level by
+// level, and a tile waits (producer, before its first TMA load) on per-matrix
+// completion counters that the epilogue warps release, so one matrix's next
+// phase starts as soon as its own inputs are complete.
 //
 // Roles per CTA (576 threads, one CTA per SM):
 //   warps 0-15 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
@@ -155,6 +162,19 @@ __device__ __forceinline__ void store32_stream(float* p, int64_t off, int nv, co
             if (k < nv) __stcs(p + off + k, v[k]);
     }
 }
+// bf16 Gram entries written by other CTAs of the same launch: read at L2
+// (ld.global.cg), never from a non-coherent cache.
+__device__ __forceinline__ void load32_bf16_l2(const bf16* p, int64_t off, int nv, float (&v)[32]) {
+    if (nv == 32) {
+        const uint4* s = reinterpret_cast<const uint4*>(p + off);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unpack_bf16x8(__ldcg(s + q), &v[8 * q]);
+    } else {
+        const unsigned short* h = reinterpret_cast<const unsigned short*>(p + off);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = k < nv ? __uint_as_float(static_cast<uint32_t>(__ldcg(h + k)) << 16) : 0.f;
+    }
+}
 __device__ __forceinline__ float load1(const void* p, int dt, int64_t off) {
     return dt == MO_F32 ? static_cast<const float*>(p)[off] : __bfloat162float(static_cast<const bf16*>(p)[off]);
 }
@@ -190,22 +210,22 @@ __device__ __forceinline__ void user_store32(const MatDesc& md, void* p, int dt,
 
 // ------------------------------------------------------------- epilogues
 // Symmetric phases: keep elements with j >= i, store at (i, j) and (j, i).
-__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int i, int j0,
-                                              float (&v)[32]) {
+__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int phase, int step, int i,
+                                              int j0, float (&v)[32]) {
     const int m = md.m;
     if (j0 + 31 < i || j0 >= m) return;
-    bf16* dst = static_cast<bf16*>(p.phase == kGram ? md.gram : md.poly);
+    bf16* dst = static_cast<bf16*>(phase == kGram ? md.gram : md.poly);
     const int nv = min(32, m - j0);
-    if (p.phase == kGram) {
-        const float sc = p.step == 0 ? md.scales[1] : 1.f;
+    if (phase == kGram) {
+        const float sc = step == 0 ? md.scales[1] : 1.f;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] *= sc;
     } else {
         float a[32];
-        load32(md.gram, MO_BF16, static_cast<int64_t>(i) * md.lda + j0, nv, a);
+        load32_bf16_l2(static_cast<const bf16*>(md.gram), static_cast<int64_t>(i) * md.lda + j0, nv, a);
         // step 0 folds the spectral scale into the coefficients (1 otherwise)
-        const float bs = p.step == 0 ? p.b * md.scales[2] : p.b;
-        const float cs = p.step == 0 ? p.c * md.scales[3] : p.c;
+        const float bs = step == 0 ? p.b * md.scales[2] : p.b;
+        const float cs = step == 0 ? p.c * md.scales[3] : p.c;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = fmaf(cs, v[k], bs * a[k]);
     }
@@ -260,13 +280,13 @@ __device__ __forceinline__ void epi_sign_pack(const MatDesc& md, int i, bool row
 
 // Called by all 32 lanes of a warp (the fused pack takes warp ballots);
 // lanes whose row lies beyond the matrix touch no memory.
-__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int i, bool row_ok, int j0,
-                                          float (&v)[32]) {
+__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int step, int i, bool row_ok,
+                                          int j0, float (&v)[32]) {
     const int n = md.n;
     if (j0 >= n) return;
     const int nv = row_ok ? min(32, n - j0) : 0;
     float x[32];
-    if (p.step == 0) {
+    if (step == 0) {
         user_load32(md, md.src, md.src_dtype, i, j0, nv, x);
         const float inv_s = md.scales[0] * md.scales[4];      // 1/||M||_F (x 1/sigma_hat when spectral)
 #pragma unroll
@@ -276,11 +296,11 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
     }
-    if (p.step + 1 < p.steps) {
+    if (step + 1 < p.steps) {
         if (!row_ok) return;
         const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
         store32_stream(md.x_master, off, nv, x);
-        store32(md.x_op[(p.step + 1) & 1], MO_BF16, off, nv, x);
+        store32(md.x_op[(step + 1) & 1], MO_BF16, off, nv, x);
         return;
     }
     if (md.sign_words != nullptr) {
@@ -298,6 +318,72 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     } else if (md.out != nullptr) {
         user_store32(md, md.out, md.out_dtype, i, j0, nv, x);
     }
+}
+
+// ------------------------------------------------- fused-launch dependencies
+// A fused launch runs several (step, phase) levels; a tile of level (t, ph)
+// of matrix md may start once, within this launch, every tile it reads or
+// overwrites the inputs of has finished:
+//   Gram(t)  reads X_t from Apply(t-1) and overwrites A, read by Poly(t-1);
+//   Poly(t)  reads A_t from Gram(t) and overwrites B, read by Apply(t-1);
+//   Apply(t) reads B_t from Poly(t), X_t from Apply(t-1), and overwrites the
+//            other X operand, read by Gram(t-1) and Apply(t-1).
+// Each epilogue warp releases one count per finished tile, so phase ph of
+// step s is complete when its counter reaches (its tiles x kEpiWarps) times
+// the number of its steps up to s that this launch runs.  The counters are
+// per matrix (mode 1), or one set over all matrices (mode 2: each level then
+// waits for the whole previous level, a grid-wide barrier per phase).
+struct Deps {
+    int* cnt;                 // [3] completion counters
+    int nt_sym, nt_apply;     // tiles they count per symmetric / apply level
+};
+__device__ __forceinline__ Deps deps_of(const NsLaunch& p, const MatDesc& md) {
+    return p.deps == 2 ? Deps{p.level_deps, p.tot_sym, p.tot_apply} : Deps{md.deps, md.nt_sym, md.nt_apply};
+}
+
+__device__ __forceinline__ int dep_need(const NsLaunch& p, const Deps& d, int ph, int upto) {
+    const int first = (p.lv_begin - ph + 2) / 3;      // first step of phase ph in this launch
+    const int cnt = upto - first + 1;
+    return cnt <= 0 ? 0 : cnt * (ph == kApply ? d.nt_apply : d.nt_sym) * kEpiWarps;
+}
+
+// Returns 1 when the dependencies were already met, 2 after spinning, 0 on
+// timeout / abort; *waited_ns accumulates the time spent spinning.
+__device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, int step, volatile int* abort_flag,
+                                      unsigned long long* waited_ns) {
+    const int need_g = dep_need(p, d, kGram, ph == kGram ? step - 1 : step);
+    const int need_p = dep_need(p, d, kPoly, ph == kApply ? step : step - 1);
+    const int need_a = dep_need(p, d, kApply, step - 1);
+    long long t0 = 0;
+    unsigned long long g0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        const bool ready = (need_g == 0 || ld_acquire_gpu(d.cnt + kGram) >= need_g) &&
+                           (need_p == 0 || ld_acquire_gpu(d.cnt + kPoly) >= need_p) &&
+                           (need_a == 0 || ld_acquire_gpu(d.cnt + kApply) >= need_a);
+        if (ready) {
+            if (it == 0) return 1;
+            *waited_ns += globaltimer_ns() - g0;
+            return 2;
+        }
+        if (it == 0) {
+            t0 = clock64();
+            g0 = globaltimer_ns();
+        }
+        if (*abort_flag || *static_cast<volatile int*>(p.err) != 0) {
+            *abort_flag = 1;
+            return 0;
+        }
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicCAS(p.err, 0, 0x105);
+            return 0;
+        }
+        __nanosleep(100);
+    }
+}
+
+__device__ __forceinline__ int2 cta_tiles(const NsLaunch& p, int ph) {
+    return static_cast<int>(blockIdx.x) < p.tc_ctas[ph] ? p.tc_ranges[ph][blockIdx.x] : make_int2(0, 0);
 }
 
 }  // namespace
@@ -330,9 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
-    const int2 range = p.cta_range[blockIdx.x];
-    const bool mn_b = p.phase == kApply;
-    if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[2 * blockIdx.x] = globaltimer_ns();
+    if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[4 * blockIdx.x] = globaltimer_ns();
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -340,40 +424,59 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             uint32_t phase = 0;
             uint32_t armed[kStages] = {0, 0, 0, 0};
             bool ok = true;
-            for (int t = 0; t < range.y && ok; ++t) {
-                const TileDesc td = p.tiles[range.x + t];
-                const MatDesc& md = p.mats[td.mat];
-                const int i0 = td.ti * kTcBM, j0 = td.tj * kTcBN;
-                const CUtensorMap* tma;
-                const CUtensorMap* tmb;
-                if (p.phase == kGram) {
-                    tma = tmb = md.tm_x[p.step & 1];
-                } else if (p.phase == kPoly) {
-                    tma = tmb = md.tm_gram;
-                } else {
-                    tma = md.tm_poly;
-                    tmb = md.tm_x[p.step & 1];
-                }
-                for (int kb = 0; kb < td.nkb; ++kb) {
-                    const uint32_t empty = smem_u32(&ctl->empty[stage]);
-                    const uint32_t full = smem_u32(&ctl->full[stage]);
-                    if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) { ok = false; break; }
-                    mbar_arrive_expect_tx(full, kStageBytes);
-                    ++armed[stage];
-                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sb = sa + kABytes;
-                    const int k0 = kb * kTcBK;
-                    tma_load_2d(sa, tma, full, k0, i0);
-                    tma_load_2d(sa + kBoxBytes, tma, full, k0, i0 + kBox);
-                    if (!mn_b) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, k0, j0 + q * kBox);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, j0 + q * kBox, k0);
+            unsigned long long dep_wait_ns = 0, dep_spins = 0;
+            for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
+                const int ph = lv % 3, step = lv / 3;
+                const int2 range = cta_tiles(p, ph);
+                const bool mn_b = ph == kApply;
+                int dep_key = -1;                    // counter set last seen met at this level
+                for (int t = 0; t < range.y && ok; ++t) {
+                    const TileDesc td = p.tc_tiles[ph][range.x + t];
+                    const MatDesc& md = p.mats[td.mat];
+                    const int key = p.deps == 2 ? 0 : td.mat;
+                    if (p.deps && key != dep_key) {
+                        const int w = wait_deps(p, deps_of(p, md), ph, step, abort_flag, &dep_wait_ns);
+                        if (w == 0) { ok = false; break; }
+                        dep_spins += w == 2;
+                        fence_proxy_async_global();
+                        dep_key = key;
                     }
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    const int i0 = td.ti * kTcBM, j0 = td.tj * kTcBN;
+                    const CUtensorMap* tma;
+                    const CUtensorMap* tmb;
+                    if (ph == kGram) {
+                        tma = tmb = md.tm_x[step & 1];
+                    } else if (ph == kPoly) {
+                        tma = tmb = md.tm_gram;
+                    } else {
+                        tma = md.tm_poly;
+                        tmb = md.tm_x[step & 1];
+                    }
+                    for (int kb = 0; kb < td.nkb; ++kb) {
+                        const uint32_t empty = smem_u32(&ctl->empty[stage]);
+                        const uint32_t full = smem_u32(&ctl->full[stage]);
+                        if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) { ok = false; break; }
+                        mbar_arrive_expect_tx(full, kStageBytes);
+                        ++armed[stage];
+                        const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                        const uint32_t sb = sa + kABytes;
+                        const int k0 = kb * kTcBK;
+                        tma_load_2d(sa, tma, full, k0, i0);
+                        tma_load_2d(sa + kBoxBytes, tma, full, k0, i0 + kBox);
+                        if (!mn_b) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, k0, j0 + q * kBox);
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, j0 + q * kBox, k0);
+                        }
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    }
                 }
+            }
+            if (p.stamps != nullptr) {
+                p.stamps[4 * blockIdx.x + 2] = dep_wait_ns;
+                p.stamps[4 * blockIdx.x + 3] = dep_spins;
             }
             if (!ok) {
                 // let every armed copy land before the CTA exits
@@ -391,36 +494,43 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int t = 0; t < range.y && ok; ++t) {
-                const TileDesc td = p.tiles[range.x + t];
-                const int acc = t & 1;
-                const uint32_t acc_phase = (t >> 1) & 1;
-                if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, abort_flag, p.err, 0x102)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d = tmem + static_cast<uint32_t>(acc * kTcBN);
-                for (int kb = 0; kb < td.nkb; ++kb) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, p.err, 0x103)) {
+            int q = 0;                                // tiles so far: accumulator ping-pong
+            for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
+                const int ph = lv % 3;
+                const int2 range = cta_tiles(p, ph);
+                const bool mn_b = ph == kApply;
+                const uint32_t idesc = mn_b ? p.idesc_apply : p.idesc_sym;
+                for (int t = 0; t < range.y && ok; ++t, ++q) {
+                    const TileDesc td = p.tc_tiles[ph][range.x + t];
+                    const int acc = q & 1;
+                    const uint32_t acc_phase = (q >> 1) & 1;
+                    if (!mbar_wait_bounded(smem_u32(&ctl->tempty[acc]), acc_phase ^ 1u, abort_flag, p.err, 0x102)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sb = sa + kABytes;
+                    const uint32_t d = tmem + static_cast<uint32_t>(acc * kTcBN);
+                    for (int kb = 0; kb < td.nkb; ++kb) {
+                        if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, p.err, 0x103)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                        const uint32_t sb = sa + kABytes;
 #pragma unroll
-                    for (int k = 0; k < kTcBK / 16; ++k) {
-                        const uint64_t ad = sdesc_sw128(sa + k * 32, 16, 1024);
-                        const uint64_t bd = mn_b ? sdesc_sw128(sb + k * 16 * 128, p.mn_lbo, p.mn_sbo)
-                                                 : sdesc_sw128(sb + k * 32, 16, 1024);
-                        umma_bf16(d, ad, bd, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < kTcBK / 16; ++k) {
+                            const uint64_t ad = sdesc_sw128(sa + k * 32, 16, 1024);
+                            const uint64_t bd = mn_b ? sdesc_sw128(sb + k * 16 * 128, p.mn_lbo, p.mn_sbo)
+                                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+                            umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        }
+                        umma_commit(smem_u32(&ctl->empty[stage]));
+                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
                     }
-                    umma_commit(smem_u32(&ctl->empty[stage]));
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    if (!ok) break;
+                    umma_commit(smem_u32(&ctl->tfull[acc]));
                 }
-                if (!ok) break;
-                umma_commit(smem_u32(&ctl->tfull[acc]));
             }
             // all issued MMAs complete before TMEM is released
             umma_commit(smem_u32(&ctl->drain));
@@ -429,44 +539,59 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
         }
     } else {
         const int quarter = warp & 3, slice = warp >> 2;
-        for (int t = 0; t < range.y; ++t) {
-            const TileDesc td = p.tiles[range.x + t];
-            const MatDesc& md = p.mats[td.mat];
-            const int acc = t & 1;
-            const uint32_t acc_phase = (t >> 1) & 1;
-            const bool ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104);
-            if (!__all_sync(0xffffffffu, ok)) break;                     // warp-uniform exit
-            tc_fence_after();
-            const int i = td.ti * kTcBM + quarter * 32 + lane;
-            const bool row_ok = i < md.m;
+        bool ok = true;
+        int q = 0;
+        for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
+            const int ph = lv % 3, step = lv / 3;
+            const int2 range = cta_tiles(p, ph);
+            for (int t = 0; t < range.y; ++t, ++q) {
+                const TileDesc td = p.tc_tiles[ph][range.x + t];
+                const MatDesc& md = p.mats[td.mat];
+                const int acc = q & 1;
+                const uint32_t acc_phase = (q >> 1) & 1;
+                ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }          // warp-uniform exit
+                tc_fence_after();
+                if (p.deps && ph == kPoly) {
+                    // the Gram entries read below were released by other CTAs
+                    if (lane == 0) (void)ld_acquire_gpu(deps_of(p, md).cnt + kGram);
+                    __syncwarp();
+                }
+                const int i = td.ti * kTcBM + quarter * 32 + lane;
+                const bool row_ok = i < md.m;
 #pragma unroll 1
-            for (int ch = 0; ch < kEpiSliceCols / 32; ++ch) {
-                const int col = slice * kEpiSliceCols + ch * 32;
-                uint32_t r[32];
-                __syncwarp();
-                tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(acc * kTcBN + col),
-                                   r);
-                tmem_wait_ld();
-                float v[32];
+                for (int ch = 0; ch < kEpiSliceCols / 32; ++ch) {
+                    const int col = slice * kEpiSliceCols + ch * 32;
+                    uint32_t r[32];
+                    __syncwarp();
+                    tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                           static_cast<uint32_t>(acc * kTcBN + col),
+                                       r);
+                    tmem_wait_ld();
+                    float v[32];
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-                const int j0 = td.tj * kTcBN + col;
-                if (p.phase == kApply)
-                    epi_apply(p, md, i, row_ok, j0, v);
-                else if (row_ok)
-                    epi_symmetric(p, md, i, j0, v);
+                    for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
+                    const int j0 = td.tj * kTcBN + col;
+                    if (ph == kApply)
+                        epi_apply(p, md, step, i, row_ok, j0, v);
+                    else if (row_ok)
+                        epi_symmetric(p, md, ph, step, i, j0, v);
+                }
+                tc_fence_before();
+                if (p.deps) fence_proxy_async_global();   // the stores above feed later TMA loads
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(smem_u32(&ctl->tempty[acc]));
+                    if (p.deps) red_release_gpu_add(deps_of(p, md).cnt + ph, 1);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->tempty[acc]));
         }
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[2 * blockIdx.x + 1] = globaltimer_ns();
+    if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[4 * blockIdx.x + 1] = globaltimer_ns();
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -475,8 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
 
 int tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_ns_tc_phase(const NsLaunch& p, int grid, cudaStream_t s) {
-    if (grid <= 0) return cudaSuccess;
+namespace {
+// Sets the kernel's shared-memory limit once per device ordinal.
+cudaError_t prepare_kernel() {
     static std::atomic<uint64_t> attr_set{0};   // one bit per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -487,8 +613,40 @@ cudaError_t launch_ns_tc_phase(const NsLaunch& p, int grid, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
     }
-    ns_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
-    return cudaGetLastError();
+    return cudaSuccess;
+}
+}  // namespace
+
+int tc_max_coresident_ctas() {
+    if (prepare_kernel() != cudaSuccess) return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ns_tc_kernel, kThreads, kSmemBytes) != cudaSuccess)
+        return 0;
+    return per_sm * device_sm_count();
+}
+
+// A launch with dependency waits is cooperative: the runtime then guarantees
+// that every CTA is resident at once (or refuses the launch), which the
+// cross-CTA waits rely on to make progress.
+cudaError_t launch_ns_tc(const NsLaunch& p, int grid, bool cooperative, cudaStream_t s) {
+    if (grid <= 0) return cudaSuccess;
+    cudaError_t e = prepare_kernel();
+    if (e != cudaSuccess) return e;
+    if (!cooperative) {
+        ns_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, ns_tc_kernel, p);
 }
 
 }  // namespace mo

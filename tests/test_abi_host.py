@@ -39,7 +39,7 @@ def test_struct_sizes_match_header():
     assert ctypes.sizeof(B.mo_matrix) == 64
     assert ctypes.sizeof(B.mo_muon_cfg) == 48
     assert ctypes.sizeof(B.mo_adamw_tail) == 72
-    assert ctypes.sizeof(B.mo_ns_view) == 80
+    assert ctypes.sizeof(B.mo_ns_view) == 96
 
 
 def test_status_strings(lib):
@@ -167,3 +167,27 @@ def test_debug_view_offsets_are_disjoint():
     assert spans[-1][0] + spans[-1][1] <= B.ns_workspace_bytes(shapes)
     with pytest.raises(B.MoError):
         B.mo_debug_set_mn_strides(4096, 4096)
+
+
+def test_debug_view_dependency_counters():
+    """Counter slots: one 16-byte slot per matrix, ahead of the NS buffers;
+    tile counts equal a brute-force count of 128 x 256 tiles (upper-triangle
+    tiles for the symmetric phases)."""
+    shapes = [(100, 300), (300, 100), (64, 64), (1000, 2000)]
+    views = [B.mo_debug_ns_view(shapes, i) for i in range(len(shapes))]
+    deps = [v.deps for v in views]
+    assert all(d % 16 == 0 for d in deps)
+    assert sorted(deps) == deps and all(b - a == 16 for a, b in zip(deps, deps[1:]))
+    assert max(deps) + 16 <= min(v.x_op[0] for v in views)
+    for v in views:
+        m, n = v.m, v.n
+        sym = sum(1 for I in range(-(-m // 128)) for J in range(-(-m // 256))
+                  if min(J * 256 + 255, m - 1) >= I * 128)
+        assert v.tiles_sym == sym
+        assert v.tiles_apply == -(-m // 128) * -(-n // 256)
+    lib = B.load()
+    assert lib.mo_debug_set_ns_fused(4) == B.MO_ERR_INVALID_ARG
+    assert lib.mo_debug_set_ns_fused(-1) == B.MO_ERR_INVALID_ARG
+    prev = B.mo_debug_set_ns_fused(0)
+    assert B.mo_debug_set_ns_fused(2) == 0
+    assert B.mo_debug_set_ns_fused(prev) == 2
