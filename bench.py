@@ -35,6 +35,35 @@ sys.path.insert(0, ROOT)
 METRIC = "Muon step matrices/s and NS TFLOP/s (fraction of bf16 peak); vote GB/s vs HBM"
 
 
+# DRAM bytes (read + write) per launch of the NS kernel from one ncu capture
+# (profiles/launches_llama7b_owner0.md), valid only while the sources that
+# shape the kernel and its schedule hash to the value recorded with it.
+PROFILED_TRAFFIC = {
+    ("llama7b_owner0", "fused"): {
+        "bytes_per_launch": 68.17e9 + 32.05e9,
+        "sources_sha256": "c84948847abe30e57c1770344d44a5e1e7eaf17acd352dc97c6f1e670286a25b",
+        "profile": "profiles/launches_llama7b_owner0.md",
+    },
+}
+TRAFFIC_SOURCES = ["matrix_optimizers_gb300/csrc/ns_tc.cu", "matrix_optimizers_gb300/csrc/ptx.cuh",
+                   "matrix_optimizers_gb300/csrc/internal.h", "matrix_optimizers_gb300/csrc/api.cu"]
+
+
+def _profiled_traffic(workload, ns_launch, max_matrices):
+    import hashlib
+    rec = PROFILED_TRAFFIC.get((workload, ns_launch))
+    if rec is None or max_matrices:
+        return None, None
+    h = hashlib.sha256()
+    root = os.path.dirname(os.path.abspath(__file__))
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(root, f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != rec["sources_sha256"]:
+        return None, "kernel sources changed since the ncu capture"
+    return rec["bytes_per_launch"], rec["profile"]
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -292,6 +321,7 @@ def run_gb300(args, rank, world, local_rank, dist):
     ns_tflops_kernel = flops_step * args.steps / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else None
     ns_tflops_step = flops_step / (ms_step * 1e-3) / 1e12
     sustained = peaks["bf16_tflops_sustained"]
+    traffic, traffic_src = _profiled_traffic(args.workload, args.ns_launch, args.max_matrices)
     all_ms = sum(v[1] for v in by_kind.values())
     result = {
         "metric": METRIC, "value": total_mats / (ms_step * 1e-3), "unit": "matrices/s",
@@ -319,7 +349,8 @@ def run_gb300(args, rank, world, local_rank, dist):
             "bound": "tensor", "achieved": ns_tflops_kernel, "peak": sustained, "unit": "TFLOP/s",
             "frac": (ns_tflops_kernel / sustained) if ns_tflops_kernel else None,
             "peak_source": f"{peaks['source']} bf16 sustained (the kernel runs inside a long step)",
-            "traffic": None, "launches": ns_launches, "avg_launch_ms": ns_ms / max(1, ns_launches),
+            "traffic": traffic, "traffic_source": traffic_src,
+            "launches": ns_launches, "avg_launch_ms": ns_ms / max(1, ns_launches),
             "work": "nominal 4m^2n+2m^3 flops per NS step per matrix",
         },
         "kernels": {k: {"launches": v[0], "total_ms": v[1], "share": v[1] / max(1e-9, all_ms)}
