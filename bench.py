@@ -268,6 +268,8 @@ def run_gb300(args, rank, world, local_rank, dist):
 
     from matrix_optimizers_gb300 import _binding
     _binding.mo_debug_set_ns_fused({"phases": 0, "fused-matrix": 1, "fused-level": 2, "fused": 3}[args.ns_launch])
+    if args.ns_tiles is not None:
+        _binding.mo_debug_set_ns_pair(args.ns_tiles == "pair")
 
     def step():
         if sign_muon:
@@ -338,6 +340,7 @@ def run_gb300(args, rank, world, local_rank, dist):
             "parallelism": f"owner-sharded: each GPU steps one share of a {max(8, world)}-rank owner plan",
             "precision": "bf16 tensor-core operands, fp32 accumulate / master / momentum",
             "ns_launch": args.ns_launch,
+            "ns_tiles": args.ns_tiles or "library default",
         },
         "ns_tflops": ns_tflops_step,
         "ns_frac_of_bf16_peak": ns_tflops_step / sustained,
@@ -576,6 +579,8 @@ def main():
                     help="NS iterations as one fused cooperative launch per step ordered by per-matrix "
                          "(fused-matrix) or grid-wide (fused-level) counters, or the library's choice "
                          "between them by size (fused), or one launch per phase")
+    ap.add_argument("--ns-tiles", default=None, choices=["single", "pair"],
+                    help="NS tile geometry: 128x256 per CTA or 256x256 per CTA pair (default: the library's)")
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

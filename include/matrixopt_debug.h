@@ -27,16 +27,20 @@ extern "C" {
  * After a call with steps = 1 the gram buffer holds X0 X0^T and the poly
  * buffer b*A + c*A*A of that step.
  * deps: three int32 completion counters (Gram, polynomial, apply) of a fused
- * bf16 launch; after a fused call each holds 16 x (that phase's tiles of this
- * matrix: tiles_sym for Gram and polynomial, tiles_apply for apply) x (the
- * steps of that phase the fused launch ran); all three stay 0 after a call
- * with one launch per phase. */
+ * bf16 launch with per-matrix ordering; after such a call each holds
+ * releases_per_tile x (that phase's tiles of this matrix: tiles_sym for Gram
+ * and polynomial, tiles_apply for apply) x (the steps of that phase the fused
+ * launch ran); all three stay 0 after a call with one launch per phase.  The
+ * tile counts and releases_per_tile are those of the tile geometry the
+ * library uses on the current device (128 x 256 tiles per CTA, 16 releases;
+ * or 256 x 256 tiles per CTA pair, 32 releases). */
 typedef struct {
     int64_t m, n, ldx, lda;
     int32_t transposed, precision;
     int64_t x_op[2], x_master, gram, poly;
     int64_t deps;
     int32_t tiles_sym, tiles_apply;
+    int32_t releases_per_tile, reserved;
 } mo_ns_view;
 
 int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precision,
@@ -52,6 +56,14 @@ int mo_debug_sm_count(void);
  * or (1024, 8192).  Other values give MO_ERR_INVALID_ARG.  Process-wide;
  * affects launches issued after the call. */
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
+
+/* Chooses the tile geometry of the bf16 tensor-core Newton-Schulz kernel:
+ * on = 1 runs 256 x 256 tiles on CTA pairs (clusters of 2, tcgen05
+ * cta_group::2: each CTA loads 128 rows of A and 128 columns of B) when the
+ * device can co-schedule such clusters; on = 0 runs 128 x 256 tiles on single
+ * CTAs.  Results are identical.  Returns the previous setting, or
+ * MO_ERR_INVALID_ARG for a value other than 0 / 1.  Process-wide. */
+int mo_debug_set_ns_pair(int on);
 
 /* Chooses how the bf16 tensor-core Newton-Schulz iterations are launched:
  *   1: every (step, phase) of a call in one cooperative persistent launch,

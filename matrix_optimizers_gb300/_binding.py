@@ -55,7 +55,8 @@ class mo_ns_view(ctypes.Structure):
     _fields_ = [("m", c_int64), ("n", c_int64), ("ldx", c_int64), ("lda", c_int64),
                 ("transposed", c_int32), ("precision", c_int32),
                 ("x_op", c_int64 * 2), ("x_master", c_int64), ("gram", c_int64),
-                ("poly", c_int64), ("deps", c_int64), ("tiles_sym", c_int32), ("tiles_apply", c_int32)]
+                ("poly", c_int64), ("deps", c_int64), ("tiles_sym", c_int32), ("tiles_apply", c_int32),
+                ("releases_per_tile", c_int32), ("reserved", c_int32)]
 
 
 # (name, restype, argtypes) of every exported symbol declared in include/*.h
@@ -98,6 +99,7 @@ _SIGNATURES = [
     ("mo_debug_sm_count", c_int32, []),
     ("mo_debug_set_mn_strides", c_int32, [ctypes.c_uint32, ctypes.c_uint32]),
     ("mo_debug_set_ns_fused", c_int32, [c_int32]),
+    ("mo_debug_set_ns_pair", c_int32, [c_int32]),
     ("mo_debug_cta_stamps", c_int32, [c_void_p, c_int32, c_int32, ctypes.POINTER(c_int32)]),
     ("mo_trace_enable", c_int32, [c_int32]),
     ("mo_trace_read", c_int32, [ctypes.POINTER(c_int32), ctypes.POINTER(c_float), c_int32,
@@ -350,6 +352,14 @@ def mo_debug_ns_view(shapes, index, precision=MO_NS_BF16):
 
 def mo_debug_set_mn_strides(lbo, sbo):
     _check(load().mo_debug_set_mn_strides(lbo, sbo))
+
+
+def mo_debug_set_ns_pair(on):
+    """Selects 256 x 256 CTA-pair tiles (True) or 128 x 256 single-CTA tiles
+    (False) for the NS kernel; returns the previous setting."""
+    prev = load().mo_debug_set_ns_pair(1 if on else 0)
+    _check(prev if prev < 0 else 0)
+    return bool(prev)
 
 
 def mo_debug_set_ns_fused(on):

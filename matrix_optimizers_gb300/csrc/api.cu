@@ -94,6 +94,24 @@ std::atomic<int> g_ns_fused{3};
 // next phase fill the tail) wins; above it the grid-wide ordering keeps every
 // CTA on the same few matrices, which measured faster through L2 reuse.
 constexpr int64_t kPerMatrixDepsMaxSymTilesPerCta = 16;
+// 1: the tensor-core kernel runs 256 x 256 tiles on CTA pairs (cta_group::2)
+// when the device can co-schedule 2-CTA clusters; 0: 128 x 256 tiles per CTA.
+std::atomic<int> g_ns_pair{0};
+
+// Co-resident CTAs of the tensor-core kernel per device ordinal, queried once.
+std::mutex g_cap_mu;
+int g_cap[64][2];
+bool g_cap_known[64][2];
+int tc_capacity(bool pair) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lk(g_cap_mu);
+    if (!g_cap_known[dev & 63][pair]) {
+        g_cap[dev & 63][pair] = tc_max_coresident_ctas(pair);
+        g_cap_known[dev & 63][pair] = true;
+    }
+    return g_cap[dev & 63][pair];
+}
 
 // ------------------------------------------------------------- the request
 struct Job {
@@ -127,13 +145,22 @@ struct MatBufs {
 };
 
 // Counts of tiles per phase for one matrix.
-int64_t sym_tiles(int64_t m) {
+// Rows of one tensor-core output tile: 128 for a single CTA, 256 for a CTA pair.
+int64_t tile_rows(bool pair) { return pair ? 2 * kTcBM : kTcBM; }
+
+// Tiles of one symmetric phase (those that meet the upper triangle) and of
+// one apply phase of an m x n iterate.
+int64_t sym_tiles(int64_t m, bool pair = false) {
     int64_t cnt = 0;
-    const int64_t tr = ceil_div(m, kTcBM), tc = ceil_div(m, kTcBN);
+    const int64_t bm = tile_rows(pair);
+    const int64_t tr = ceil_div(m, bm), tc = ceil_div(m, kTcBN);
     for (int64_t I = 0; I < tr; ++I)
         for (int64_t J = 0; J < tc; ++J)
-            if (std::min(J * kTcBN + kTcBN - 1, m - 1) >= I * kTcBM) ++cnt;
+            if (std::min(J * kTcBN + kTcBN - 1, m - 1) >= I * bm) ++cnt;
     return cnt;
+}
+int64_t apply_tiles(int64_t m, int64_t n, bool pair = false) {
+    return ceil_div(m, tile_rows(pair)) * ceil_div(n, kTcBN);
 }
 
 struct Layout {
@@ -164,7 +191,7 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
             const int64_t st = sym_tiles(s.m);
             L.ntiles[0] += st;
             L.ntiles[1] += st;
-            L.ntiles[2] += ceil_div(s.m, kTcBM) * ceil_div(s.n, kTcBN);
+            L.ntiles[2] += apply_tiles(s.m, s.n);   // single-CTA counts bound the pair ones
         } else {
             const int64_t t = ceil_div(s.m, kFpBM);
             L.ntiles[0] += t * t;
@@ -326,20 +353,24 @@ struct Plan {
     std::vector<int64_t> key;
     Layout L;
     std::vector<uint8_t> stage;
-    int grids[3] = {0, 0, 0};
+    bool pair = false;             // tensor-core tiles for CTA pairs (cta_group::2)
+    int grids[3] = {0, 0, 0};      // schedule units (CTAs, or CTA pairs) holding tiles, per phase
+    int64_t ntiles[3] = {0, 0, 0}; // tiles per phase in this geometry
 };
 
 std::mutex g_plan_mu;
 std::vector<std::shared_ptr<const Plan>> g_plans;   // most recently used first
 constexpr size_t kPlanCacheSize = 16;
 
-std::vector<int64_t> plan_key(const std::vector<Job>& jobs, int precision, const void* ws) {
+std::vector<int64_t> plan_key(const std::vector<Job>& jobs, int precision, const void* ws, bool pair, int units) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
     std::vector<int64_t> k;
-    k.reserve(4 + jobs.size() * 13);
+    k.reserve(6 + jobs.size() * 13);
     k.push_back(dev);
     k.push_back(precision);
+    k.push_back(pair ? 1 : 0);
+    k.push_back(units);
     k.push_back(static_cast<int64_t>(reinterpret_cast<uintptr_t>(ws)));
     k.push_back(device_sm_count());
     for (const Job& j : jobs) {
@@ -354,7 +385,9 @@ std::vector<int64_t> plan_key(const std::vector<Job>& jobs, int precision, const
     return k;
 }
 
-int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::shared_ptr<Plan>& out) {
+// `units`: schedule units of the tensor-core path (CTAs, or CTA pairs when `pair`).
+int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair, int units,
+               std::shared_ptr<Plan>& out) {
     std::vector<std::pair<int64_t, int64_t>> dims;
     dims.reserve(jobs.size());
     for (const Job& j : jobs) dims.push_back({j.rows, j.cols});
@@ -364,7 +397,7 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
     if (precision == MO_NS_BF16 && !get_encode()) return MO_ERR_CUDA;
 
     uint8_t* base = static_cast<uint8_t*>(ws);
-    const int nsm = device_sm_count();
+    plan->pair = pair;
     plan->stage.assign(L.ctl_bytes, 0);
     uint8_t* h = plan->stage.data();
     const NsOpts o{precision, 0, 0, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0};
@@ -410,8 +443,8 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
         d.mom_tiles_r = static_cast<int32_t>(ceil_div(j.rows, kMomTile));
         d.mom_tiles_c = static_cast<int32_t>(ceil_div(j.cols, kMomTile));
         mom_begin += static_cast<int64_t>(d.mom_tiles_r) * d.mom_tiles_c;
-        d.nt_sym = static_cast<int32_t>(sym_tiles(s.m));
-        d.nt_apply = static_cast<int32_t>(ceil_div(s.m, kTcBM) * ceil_div(s.n, kTcBN));
+        d.nt_sym = static_cast<int32_t>(sym_tiles(s.m, pair));
+        d.nt_apply = static_cast<int32_t>(apply_tiles(s.m, s.n, pair));
         d.deps = reinterpret_cast<int*>(base + L.deps) + 4 * i;
         if (o.precision == MO_NS_BF16) {
             for (int q = 0; q < 2; ++q) {
@@ -436,7 +469,8 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
             const Shape& s = L.shape[i];
             if (o.precision == MO_NS_BF16) {
                 const int nkb = static_cast<int>(ceil_div(ph == kGram ? s.n : s.m, kTcBK));
-                const int64_t tr = ceil_div(s.m, kTcBM);
+                const int64_t bm = tile_rows(pair);
+                const int64_t tr = ceil_div(s.m, bm);
                 const int64_t tc = ceil_div(ph == kApply ? s.n : s.m, kTcBN);
                 if (ph == kApply) {
                     // column-block-major: the CTAs of one wave share a few
@@ -448,7 +482,7 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
                 } else {
                     for (int64_t I = 0; I < tr; ++I)
                         for (int64_t J = 0; J < tc; ++J) {
-                            if (std::min(J * kTcBN + kTcBN - 1, s.m - 1) < I * kTcBM) continue;
+                            if (std::min(J * kTcBN + kTcBN - 1, s.m - 1) < I * bm) continue;
                             tiles.push_back(TileDesc{static_cast<int32_t>(i), static_cast<int32_t>(I),
                                                      static_cast<int32_t>(J), nkb});
                         }
@@ -464,8 +498,9 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
             }
         }
         TileDesc* ht = reinterpret_cast<TileDesc*>(h + L.tiles[ph]);
+        plan->ntiles[ph] = static_cast<int64_t>(tiles.size());
         if (o.precision == MO_NS_BF16) {
-            const int ctas = static_cast<int>(std::min<int64_t>(nsm, static_cast<int64_t>(tiles.size())));
+            const int ctas = static_cast<int>(std::min<int64_t>(units, static_cast<int64_t>(tiles.size())));
             std::vector<TileDesc> sorted;
             std::vector<int2> ranges;
             schedule(tiles, ctas, ph == kApply ? 6 : 4, sorted, ranges);
@@ -481,8 +516,9 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, std::share
     return MO_OK;
 }
 
-int get_plan(const std::vector<Job>& jobs, int precision, void* ws, std::shared_ptr<const Plan>& out) {
-    std::vector<int64_t> key = plan_key(jobs, precision, ws);
+int get_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair, int units,
+             std::shared_ptr<const Plan>& out) {
+    std::vector<int64_t> key = plan_key(jobs, precision, ws, pair, units);
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
         for (size_t i = 0; i < g_plans.size(); ++i) {
@@ -494,7 +530,7 @@ int get_plan(const std::vector<Job>& jobs, int precision, void* ws, std::shared_
         }
     }
     std::shared_ptr<Plan> p;
-    int st = build_plan(jobs, precision, ws, p);
+    int st = build_plan(jobs, precision, ws, pair, units, p);
     if (st != MO_OK) return st;
     p->key = std::move(key);
     std::lock_guard<std::mutex> lk(g_plan_mu);
@@ -510,13 +546,17 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     if (jobs.empty()) return MO_OK;
     int st = validate_ws(ws, ws_bytes, 0);
     if (st != MO_OK) return st;
+    const bool tc = o.precision == MO_NS_BF16;
+    const int nsm = device_sm_count();
+    const bool pair = tc && g_ns_pair.load() != 0 && tc_capacity(true) >= 2;
+    const int units = pair ? std::min(nsm / 2, tc_capacity(true) / 2) : nsm;
+    const int cta_per_unit = pair ? 2 : 1;
     std::shared_ptr<const Plan> plan;
-    if ((st = get_plan(jobs, o.precision, ws, plan)) != MO_OK) return st;
+    if ((st = get_plan(jobs, o.precision, ws, pair, units, plan)) != MO_OK) return st;
     const Layout& L = plan->L;
     if ((st = validate_ws(ws, ws_bytes, L.total)) != MO_OK) return st;
     const int* grids = plan->grids;
     uint8_t* base = static_cast<uint8_t*>(ws);
-    const int nsm = device_sm_count();
 
     cudaError_t e = cudaMemcpyAsync(base, plan->stage.data(), L.ctl_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return MO_ERR_CUDA;
@@ -553,20 +593,21 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     np.mn_lbo = g_mn_lbo.load();
     np.mn_sbo = g_mn_sbo.load();
     np.level_deps = reinterpret_cast<int*>(base + L.deps) + 4 * jobs.size();
-    np.tot_sym = static_cast<int32_t>(L.ntiles[kGram]);
-    np.tot_apply = static_cast<int32_t>(L.ntiles[kApply]);
-    np.idesc_sym = idesc_bf16_f32(kTcBM, kTcBN, 0u);
-    np.idesc_apply = idesc_bf16_f32(kTcBM, kTcBN, 1u);
+    np.tot_sym = static_cast<int32_t>(plan->ntiles[kGram]);
+    np.tot_apply = static_cast<int32_t>(plan->ntiles[kApply]);
+    np.rel_per_tile = kTcEpiWarps * cta_per_unit;
+    const uint32_t mma_m = static_cast<uint32_t>(kTcBM * cta_per_unit);
+    np.idesc_sym = idesc_bf16_f32(mma_m, kTcBN, 0u);
+    np.idesc_apply = idesc_bf16_f32(mma_m, kTcBN, 1u);
     for (int ph = 0; ph < 3; ++ph) {
         np.tc_tiles[ph] = reinterpret_cast<const TileDesc*>(base + L.tiles[ph]);
         np.tc_ranges[ph] = reinterpret_cast<const int2*>(base + L.ranges[ph]);
         np.tc_ctas[ph] = grids[ph];
     }
-    const bool tc = o.precision == MO_NS_BF16;
     const int levels = 3 * o.steps;
-    const int grid_fused = std::max(grids[0], std::max(grids[1], grids[2]));
+    const int units_fused = std::max(grids[0], std::max(grids[1], grids[2]));
     int mode = g_ns_fused.load();             // 0 per-phase, 1 / 2 fused (counter granularity)
-    if (mode == 3) mode = L.ntiles[kGram] < kPerMatrixDepsMaxSymTilesPerCta * grid_fused ? 1 : 2;
+    if (mode == 3) mode = plan->ntiles[kGram] < kPerMatrixDepsMaxSymTilesPerCta * units_fused ? 1 : 2;
 
     // one launch of levels [lv0, lv1): the per-phase form, or the fused one
     auto launch_levels = [&](int lv0, int lv1) -> cudaError_t {
@@ -578,20 +619,19 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
         np.step = lv0 / 3;
         np.tiles = reinterpret_cast<const TileDesc*>(base + L.tiles[np.phase]);
         np.ntiles = static_cast<int32_t>(L.ntiles[np.phase]);
-        const int grid = fused ? grid_fused : grids[np.phase];
+        const int grid = (fused ? units_fused : grids[np.phase]) * (tc ? cta_per_unit : 1);
         np.stamps = nullptr;
         Stamps& sp = t_stamps;
         if (tc && sp.buf != nullptr && sp.count < sp.capacity && grid <= sp.max_ctas)
             np.stamps = sp.buf + 4 * static_cast<int64_t>(sp.count++) * sp.max_ctas;
         return traced(fused ? MO_K_NS_FUSED : MO_K_GRAM + np.phase, stream, [&] {
-            return tc ? launch_ns_tc(np, grid, fused, stream) : launch_ns_fp32_phase(np, grid, stream);
+            return tc ? launch_ns_tc(np, grid, fused, pair, stream) : launch_ns_fp32_phase(np, grid, stream);
         });
     };
 
     // the spectral estimate runs between the first Gram phase and the rest
     const int lv_fuse = o.spectral_iters > 0 ? 1 : 0;
-    const bool fuse = tc && mode != 0 && levels - lv_fuse > 1 &&
-                      grid_fused <= tc_max_coresident_ctas();
+    const bool fuse = tc && mode != 0 && levels - lv_fuse > 1 && units_fused * cta_per_unit <= tc_capacity(pair);
     for (int lv = 0; lv < levels;) {
         const int lv1 = fuse && lv >= lv_fuse ? levels : lv + 1;
         if ((e = launch_levels(lv, lv1)) != cudaSuccess) return MO_ERR_CUDA;
@@ -1034,8 +1074,11 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
     view->gram = static_cast<int64_t>(b.gram);
     view->poly = static_cast<int64_t>(b.poly);
     view->deps = static_cast<int64_t>(L.deps + 4 * sizeof(int) * static_cast<size_t>(active));
-    view->tiles_sym = static_cast<int32_t>(sym_tiles(s.m));
-    view->tiles_apply = static_cast<int32_t>(ceil_div(s.m, kTcBM) * ceil_div(s.n, kTcBN));
+    const bool pair = precision == MO_NS_BF16 && g_ns_pair.load() != 0 && tc_capacity(true) >= 2;
+    view->tiles_sym = static_cast<int32_t>(sym_tiles(s.m, pair));
+    view->tiles_apply = static_cast<int32_t>(apply_tiles(s.m, s.n, pair));
+    view->releases_per_tile = kTcEpiWarps * (pair ? 2 : 1);
+    view->reserved = 0;
     return MO_OK;
 }
 
@@ -1090,6 +1133,11 @@ int mo_trace_read(int32_t* kinds, float* ms, int cap, int* count) {
     *count = t.count;
     t.count = 0;
     return MO_OK;
+}
+
+int mo_debug_set_ns_pair(int on) {
+    if (on != 0 && on != 1) return MO_ERR_INVALID_ARG;
+    return g_ns_pair.exchange(on);
 }
 
 int mo_debug_set_ns_fused(int on) {

@@ -14,6 +14,7 @@ namespace mo {
 constexpr int kTcBM = 128;   // rows of D per tile (TMEM lanes)
 constexpr int kTcBN = 256;   // columns of D per tile (TMEM columns per accumulator)
 constexpr int kTcBK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int kTcEpiWarps = 16;   // epilogue warps per CTA of the tensor-core kernel
 // Tile geometry of the CUDA-core fp32 GEMM.
 constexpr int kFpBM = 64, kFpBN = 64, kFpBK = 16;
 // Momentum / normalisation kernel tile.
@@ -98,6 +99,7 @@ struct NsLaunch {
                                // counter set (every tile of a level waits for the whole previous level)
     int* level_deps;           // [3] the grid-wide counters of mode 2
     int32_t tot_sym, tot_apply;  // tiles of one symmetric / apply level over all matrices
+    int32_t rel_per_tile;      // counter releases per finished tile (16 epilogue warps per CTA)
     uint32_t idesc_sym, idesc_apply;
     uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
     unsigned long long* stamps;  // null, or [4 * gridDim.x]: per CTA start / end %globaltimer (ns),
@@ -119,8 +121,9 @@ cudaError_t launch_norm_finalize(const MatDesc* mats, int nmats, const float* pa
                                  cudaStream_t s);
 cudaError_t launch_ns_k0(const MomLaunch& p, float alpha, float decay, int apply_update, int grid,
                          cudaStream_t s);
-cudaError_t launch_ns_tc(const NsLaunch& p, int grid, bool cooperative, cudaStream_t s);
-int tc_max_coresident_ctas();   // CTAs of the tensor-core kernel that fit on the device at once
+// pair: the 2-CTA (cta_group::2) form, grid = 2 x CTA pairs
+cudaError_t launch_ns_tc(const NsLaunch& p, int grid, bool cooperative, bool pair, cudaStream_t s);
+int tc_max_coresident_ctas(bool pair);   // CTAs of that form that fit on the device at once
 cudaError_t launch_ns_fp32_phase(const NsLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_sign_pack(const void* U, int dtype, int64_t rows, int64_t cols, int64_t ld,
                              uint32_t* words, cudaStream_t s);
@@ -139,7 +142,7 @@ cudaError_t launch_sign_int8(const void* U, int dtype, int64_t rows, int64_t col
 cudaError_t launch_vote_int8(const int8_t* const* signs, int M, int64_t rows, int64_t cols, void* W, int w_dtype,
                              int64_t ld, float lr, cudaStream_t s);
 
-int tc_smem_bytes();
+int tc_smem_bytes(bool pair);
 int device_sm_count();
 
 }  // namespace mo

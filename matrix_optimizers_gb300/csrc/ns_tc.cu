@@ -41,23 +41,38 @@ using bf16 = __nv_bfloat16;
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kBox = 64;                                   // TMA box edge (elements)
 constexpr int kBoxBytes = kBox * kBox * 2;                 // 8 KB
-constexpr int kABytes = kTcBM * kTcBK * 2;                 // 16 KB
-constexpr int kBBytes = kTcBN * kTcBK * 2;                 // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kEpiWarps = 16;                              // 4 lane quarters x 4 column slices
+constexpr int kABytes = kTcBM * kTcBK * 2;                 // 16 KB: 128 rows of A per CTA
+constexpr int kEpiWarps = kTcEpiWarps;                     // 4 lane quarters x 4 column slices
 constexpr int kEpiSliceCols = kTcBN / (kEpiWarps / 4);     // 64 accumulator columns per epilogue warp
 constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+constexpr int kMaxStages = 6;
+
+// Tile geometry.  Single CTA (cta_group::1): a 128 x 256 tile per CTA, the
+// stage holding 128 rows of A and all 256 columns of B.  CTA pair
+// (cta_group::2, cluster of 2): a 256 x 256 tile per pair; each CTA holds 128
+// rows of A, 128 columns of B and its own 128 x 256 accumulator, so a stage
+// is 32 KB and the ring is six deep.
+template <bool kPair>
+struct Geo {
+    static constexpr int kStages = kPair ? 6 : 4;
+    static constexpr int kBBoxes = kPair ? 2 : 4;            // 64-wide B boxes per CTA and stage
+    static constexpr int kStageBytes = kABytes + kBBoxes * kBoxBytes;
+    static constexpr int kTileRows = kPair ? 2 * kTcBM : kTcBM;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+    static constexpr int kTxBytes = (kPair ? 2 : 1) * kStageBytes;   // counted on the leader's full barrier
+    static constexpr uint32_t kTemptyCount = (kPair ? 2 : 1) * kEpiWarps;
+};
+static_assert(Geo<true>::kStages <= kMaxStages && Geo<false>::kStages <= kMaxStages, "ring depth");
+static_assert(Geo<true>::kSmemBytes <= 232448 && Geo<false>::kSmemBytes <= 232448, "shared memory");
 
 struct Ctl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -328,8 +343,9 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
 //   Poly(t)  reads A_t from Gram(t) and overwrites B, read by Apply(t-1);
 //   Apply(t) reads B_t from Poly(t), X_t from Apply(t-1), and overwrites the
 //            other X operand, read by Gram(t-1) and Apply(t-1).
-// Each epilogue warp releases one count per finished tile, so phase ph of
-// step s is complete when its counter reaches (its tiles x kEpiWarps) times
+// Each epilogue warp releases one count per finished tile (16 per CTA, so 16
+// or 32 per tile), so phase ph of step s is complete when its counter reaches
+// (its tiles x releases per tile) times
 // the number of its steps up to s that this launch runs.  The counters are
 // per matrix (mode 1), or one set over all matrices (mode 2: each level then
 // waits for the whole previous level, a grid-wide barrier per phase).
@@ -344,7 +360,7 @@ __device__ __forceinline__ Deps deps_of(const NsLaunch& p, const MatDesc& md) {
 __device__ __forceinline__ int dep_need(const NsLaunch& p, const Deps& d, int ph, int upto) {
     const int first = (p.lv_begin - ph + 2) / 3;      // first step of phase ph in this launch
     const int cnt = upto - first + 1;
-    return cnt <= 0 ? 0 : cnt * (ph == kApply ? d.nt_apply : d.nt_sym) * kEpiWarps;
+    return cnt <= 0 ? 0 : cnt * (ph == kApply ? d.nt_apply : d.nt_sym) * p.rel_per_tile;
 }
 
 // Returns 1 when the dependencies were already met, 2 after spinning, 0 on
@@ -382,37 +398,50 @@ __device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, 
     }
 }
 
-__device__ __forceinline__ int2 cta_tiles(const NsLaunch& p, int ph) {
-    return static_cast<int>(blockIdx.x) < p.tc_ctas[ph] ? p.tc_ranges[ph][blockIdx.x] : make_int2(0, 0);
+// Tiles of phase ph scheduled on schedule unit `unit` (a CTA, or a CTA pair).
+__device__ __forceinline__ int2 unit_tiles(const NsLaunch& p, int ph, int unit) {
+    return unit < p.tc_ctas[ph] ? p.tc_ranges[ph][unit] : make_int2(0, 0);
 }
 
 }  // namespace
 
+
+template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constant__ NsLaunch p) {
+    using G = Geo<kPair>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Ctl* ctl = reinterpret_cast<Ctl*>(smem + kStages * kStageBytes);
+    Ctl* ctl = reinterpret_cast<Ctl*>(smem + G::kStages * G::kStageBytes);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? cluster_ctarank() : 0u;      // rank 0 leads the pair
+    const bool leader = rank == 0;
+    const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < G::kStages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&ctl->tfull[a]), 1);
-            mbar_init(smem_u32(&ctl->tempty[a]), kEpiWarps);
+            mbar_init(smem_u32(&ctl->tempty[a]), G::kTemptyCount);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish();
+        if constexpr (kPair) {
+            tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();          // both CTAs' barriers exist before any remote signal
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int* abort_flag = &ctl->abort_flag;
@@ -422,12 +451,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t armed[kStages] = {0, 0, 0, 0};
+            uint32_t armed[G::kStages];
+            for (int s = 0; s < G::kStages; ++s) armed[s] = 0;
             bool ok = true;
             unsigned long long dep_wait_ns = 0, dep_spins = 0;
             for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
                 const int ph = lv % 3, step = lv / 3;
-                const int2 range = cta_tiles(p, ph);
+                const int2 range = unit_tiles(p, ph, unit);
                 const bool mn_b = ph == kApply;
                 int dep_key = -1;                    // counter set last seen met at this level
                 for (int t = 0; t < range.y && ok; ++t) {
@@ -441,7 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         fence_proxy_async_global();
                         dep_key = key;
                     }
-                    const int i0 = td.ti * kTcBM, j0 = td.tj * kTcBN;
+                    // this CTA's rows of A and columns of B
+                    const int i0 = td.ti * G::kTileRows + static_cast<int>(rank) * kTcBM;
+                    const int j0 = td.tj * kTcBN + (kPair ? static_cast<int>(rank) * (kTcBN / 2) : 0);
                     const CUtensorMap* tma;
                     const CUtensorMap* tmb;
                     if (ph == kGram) {
@@ -456,21 +488,41 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         const uint32_t empty = smem_u32(&ctl->empty[stage]);
                         const uint32_t full = smem_u32(&ctl->full[stage]);
                         if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) { ok = false; break; }
-                        mbar_arrive_expect_tx(full, kStageBytes);
+                        if (leader) mbar_arrive_expect_tx(full, G::kTxBytes);
                         ++armed[stage];
-                        const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                        const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
                         const uint32_t sb = sa + kABytes;
                         const int k0 = kb * kTcBK;
-                        tma_load_2d(sa, tma, full, k0, i0);
-                        tma_load_2d(sa + kBoxBytes, tma, full, k0, i0 + kBox);
-                        if (!mn_b) {
+                        // (the operand-major test stays outside the unrolled box loops: a
+                        // branch between the copies measured ~20% slower in every phase,
+                        // the producer thread's issue rate being on the critical path)
+                        if constexpr (kPair) {
+                            const uint32_t bar = mapa_shared(full, 0);   // the leader's barrier
+                            tma_load_2d_pair(sa, tma, bar, k0, i0);
+                            tma_load_2d_pair(sa + kBoxBytes, tma, bar, k0, i0 + kBox);
+                            if (!mn_b) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, k0, j0 + q * kBox);
+                                for (int q = 0; q < G::kBBoxes; ++q)
+                                    tma_load_2d_pair(sb + q * kBoxBytes, tmb, bar, k0, j0 + q * kBox);
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < G::kBBoxes; ++q)
+                                    tma_load_2d_pair(sb + q * kBoxBytes, tmb, bar, j0 + q * kBox, k0);
+                            }
                         } else {
+                            tma_load_2d(sa, tma, full, k0, i0);
+                            tma_load_2d(sa + kBoxBytes, tma, full, k0, i0 + kBox);
+                            if (!mn_b) {
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) tma_load_2d(sb + q * kBoxBytes, tmb, full, j0 + q * kBox, k0);
+                                for (int q = 0; q < G::kBBoxes; ++q)
+                                    tma_load_2d(sb + q * kBoxBytes, tmb, full, k0, j0 + q * kBox);
+                            } else {
+#pragma unroll
+                                for (int q = 0; q < G::kBBoxes; ++q)
+                                    tma_load_2d(sb + q * kBoxBytes, tmb, full, j0 + q * kBox, k0);
+                            }
                         }
-                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                        if (++stage == G::kStages) { stage = 0; phase ^= 1u; }
                     }
                 }
             }
@@ -479,25 +531,32 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 p.stamps[4 * blockIdx.x + 3] = dep_spins;
             }
             if (!ok) {
-                // let every armed copy land before the CTA exits
-                for (int s = 0; s < kStages; ++s) {
-                    if (armed[s] == 0) continue;
-                    const uint32_t full = smem_u32(&ctl->full[s]);
-                    const uint32_t par = (armed[s] - 1u) & 1u;
+                if (leader) {
+                    // let every armed copy land before the CTA exits
+                    for (int s = 0; s < G::kStages; ++s) {
+                        if (armed[s] == 0) continue;
+                        const uint32_t full = smem_u32(&ctl->full[s]);
+                        const uint32_t par = (armed[s] - 1u) & 1u;
+                        long long t0 = clock64();
+                        while (!mbar_try_wait(full, par) && clock64() - t0 < kWaitCycles) {}
+                    }
+                } else {
+                    // the peer's copies complete on the leader's barriers: give
+                    // those in flight time to land (far above a copy's latency)
                     long long t0 = clock64();
-                    while (!mbar_try_wait(full, par) && clock64() - t0 < kWaitCycles) {}
+                    while (clock64() - t0 < (1LL << 22)) {}
                 }
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
             int q = 0;                                // tiles so far: accumulator ping-pong
             for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
                 const int ph = lv % 3;
-                const int2 range = cta_tiles(p, ph);
+                const int2 range = unit_tiles(p, ph, unit);
                 const bool mn_b = ph == kApply;
                 const uint32_t idesc = mn_b ? p.idesc_apply : p.idesc_sym;
                 for (int t = 0; t < range.y && ok; ++t, ++q) {
@@ -516,34 +575,52 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+                        const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
                         const uint32_t sb = sa + kABytes;
 #pragma unroll
                         for (int k = 0; k < kTcBK / 16; ++k) {
                             const uint64_t ad = sdesc_sw128(sa + k * 32, 16, 1024);
                             const uint64_t bd = mn_b ? sdesc_sw128(sb + k * 16 * 128, p.mn_lbo, p.mn_sbo)
                                                      : sdesc_sw128(sb + k * 32, 16, 1024);
-                            umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                            if constexpr (kPair)
+                                umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                            else
+                                umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                         }
-                        umma_commit(smem_u32(&ctl->empty[stage]));
-                        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                        if constexpr (kPair)
+                            umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
+                        else
+                            umma_commit(smem_u32(&ctl->empty[stage]));
+                        if (++stage == G::kStages) { stage = 0; phase ^= 1u; }
                     }
                     if (!ok) break;
-                    umma_commit(smem_u32(&ctl->tfull[acc]));
+                    if constexpr (kPair)
+                        umma_commit_pair(smem_u32(&ctl->tfull[acc]), 0x3);
+                    else
+                        umma_commit(smem_u32(&ctl->tfull[acc]));
                 }
             }
-            // all issued MMAs complete before TMEM is released
-            umma_commit(smem_u32(&ctl->drain));
+            // all issued MMAs complete before TMEM is released (in both CTAs of a pair)
+            if constexpr (kPair)
+                umma_commit_pair(smem_u32(&ctl->drain), 0x3);
+            else
+                umma_commit(smem_u32(&ctl->drain));
+            long long t0 = clock64();
+            while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < kWaitCycles) {}
+        } else if (kPair && lane == 0) {
+            // the peer's accumulators are written by the leader's MMAs
             long long t0 = clock64();
             while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < kWaitCycles) {}
         }
     } else {
         const int quarter = warp & 3, slice = warp >> 2;
+        const uint32_t tempty_leader[2] = {kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0) : 0u,
+                                           kPair ? mapa_shared(smem_u32(&ctl->tempty[1]), 0) : 0u};
         bool ok = true;
         int q = 0;
         for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
             const int ph = lv % 3, step = lv / 3;
-            const int2 range = cta_tiles(p, ph);
+            const int2 range = unit_tiles(p, ph, unit);
             for (int t = 0; t < range.y; ++t, ++q) {
                 const TileDesc td = p.tc_tiles[ph][range.x + t];
                 const MatDesc& md = p.mats[td.mat];
@@ -557,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     if (lane == 0) (void)ld_acquire_gpu(deps_of(p, md).cnt + kGram);
                     __syncwarp();
                 }
-                const int i = td.ti * kTcBM + quarter * 32 + lane;
+                const int i = td.ti * G::kTileRows + static_cast<int>(rank) * kTcBM + quarter * 32 + lane;
                 const bool row_ok = i < md.m;
 #pragma unroll 1
                 for (int ch = 0; ch < kEpiSliceCols / 32; ++ch) {
@@ -581,7 +658,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 if (p.deps) fence_proxy_async_global();   // the stores above feed later TMA loads
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(smem_u32(&ctl->tempty[acc]));
+                    if (leader)
+                        mbar_arrive(smem_u32(&ctl->tempty[acc]));
+                    else
+                        mbar_arrive_cluster(tempty_leader[acc]);
                     if (p.deps) red_release_gpu_add(deps_of(p, md).cnt + ph, 1);
                 }
             }
@@ -592,61 +672,94 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
     tc_fence_before();
     __syncthreads();
     if (p.stamps != nullptr && threadIdx.x == 0) p.stamps[4 * blockIdx.x + 1] = globaltimer_ns();
+    if constexpr (kPair) cluster_sync();          // neither CTA leaves while the other may signal it
     if (warp == kMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        if constexpr (kPair)
+            tmem_dealloc_pair(tmem, kTmemCols);
+        else
+            tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-int tc_smem_bytes() { return kSmemBytes; }
+int tc_smem_bytes(bool pair) { return pair ? Geo<true>::kSmemBytes : Geo<false>::kSmemBytes; }
 
 namespace {
-// Sets the kernel's shared-memory limit once per device ordinal.
-cudaError_t prepare_kernel() {
+// Sets the kernels' shared-memory limit once per device ordinal.
+cudaError_t prepare_kernels() {
     static std::atomic<uint64_t> attr_set{0};   // one bit per device ordinal
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = uint64_t(1) << (dev & 63);
     if (!(attr_set.load() & bit)) {
-        e = cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e = cudaFuncSetAttribute(ns_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Geo<false>::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(ns_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Geo<true>::kSmemBytes);
         if (e != cudaSuccess) return e;
         attr_set.fetch_or(bit);
     }
     return cudaSuccess;
 }
+
+cudaLaunchConfig_t launch_config(bool pair, int grid, cudaStream_t s, cudaLaunchAttribute* attr, bool cooperative) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = tc_smem_bytes(pair);
+    cfg.stream = s;
+    int n = 0;
+    if (pair) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cfg;
+}
 }  // namespace
 
-int tc_max_coresident_ctas() {
-    if (prepare_kernel() != cudaSuccess) return 0;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ns_tc_kernel, kThreads, kSmemBytes) != cudaSuccess)
+int tc_max_coresident_ctas(bool pair) {
+    if (prepare_kernels() != cudaSuccess) return 0;
+    if (!pair) {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ns_tc_kernel<false>, kThreads,
+                                                          Geo<false>::kSmemBytes) != cudaSuccess)
+            return 0;
+        return per_sm * device_sm_count();
+    }
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config(true, 2 * device_sm_count(), nullptr, attr, false);
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, ns_tc_kernel<true>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
         return 0;
-    return per_sm * device_sm_count();
+    }
+    return 2 * clusters;
 }
 
 // A launch with dependency waits is cooperative: the runtime then guarantees
 // that every CTA is resident at once (or refuses the launch), which the
-// cross-CTA waits rely on to make progress.
-cudaError_t launch_ns_tc(const NsLaunch& p, int grid, bool cooperative, cudaStream_t s) {
+// cross-CTA waits rely on to make progress.  A pair launch is a cluster
+// launch of 2-CTA clusters (grid even).
+cudaError_t launch_ns_tc(const NsLaunch& p, int grid, bool cooperative, bool pair, cudaStream_t s) {
     if (grid <= 0) return cudaSuccess;
-    cudaError_t e = prepare_kernel();
+    if (pair && (grid & 1)) return cudaErrorInvalidConfiguration;
+    cudaError_t e = prepare_kernels();
     if (e != cudaSuccess) return e;
-    if (!cooperative) {
-        ns_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, ns_tc_kernel, p);
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg = launch_config(pair, grid, s, attr, cooperative);
+    return pair ? cudaLaunchKernelEx(&cfg, ns_tc_kernel<true>, p) : cudaLaunchKernelEx(&cfg, ns_tc_kernel<false>, p);
 }
 
 }  // namespace mo

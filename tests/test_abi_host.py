@@ -39,7 +39,7 @@ def test_struct_sizes_match_header():
     assert ctypes.sizeof(B.mo_matrix) == 64
     assert ctypes.sizeof(B.mo_muon_cfg) == 48
     assert ctypes.sizeof(B.mo_adamw_tail) == 72
-    assert ctypes.sizeof(B.mo_ns_view) == 96
+    assert ctypes.sizeof(B.mo_ns_view) == 104
 
 
 def test_status_strings(lib):

@@ -96,7 +96,8 @@ def test_fused_counters_reach_totals(case):
         v = B.mo_debug_ns_view(shapes, i)
         cnt = ws[v.deps: v.deps + 12].view(torch.int32).cpu().tolist()
         gram_steps = steps - 1 if spectral else steps
-        assert cnt == [16 * v.tiles_sym * gram_steps, 16 * v.tiles_sym * steps, 16 * v.tiles_apply * steps], i
+        r = v.releases_per_tile
+        assert cnt == [r * v.tiles_sym * gram_steps, r * v.tiles_sym * steps, r * v.tiles_apply * steps], i
     views = [B.mo_debug_ns_view(shapes, i) for i in range(len(shapes))]
     lvl = views[-1].deps + 16                          # the grid-wide set follows the last matrix
     assert ws[lvl: lvl + 12].view(torch.int32).cpu().tolist() == [0, 0, 0]
@@ -106,8 +107,9 @@ def test_fused_counters_reach_totals(case):
         assert ws[v.deps: v.deps + 12].view(torch.int32).cpu().tolist() == [0, 0, 0]
     ts, ta = sum(v.tiles_sym for v in views), sum(v.tiles_apply for v in views)
     gram_steps = steps - 1 if spectral else steps
-    assert ws[lvl: lvl + 12].view(torch.int32).cpu().tolist() == [16 * ts * gram_steps, 16 * ts * steps,
-                                                                 16 * ta * steps]
+    r = views[0].releases_per_tile
+    assert ws[lvl: lvl + 12].view(torch.int32).cpu().tolist() == [r * ts * gram_steps, r * ts * steps,
+                                                                 r * ta * steps]
     _, _, ws, _ = _step(_inputs(shapes, 5), kw, 0)
     for v in views:
         assert ws[v.deps: v.deps + 12].view(torch.int32).cpu().tolist() == [0, 0, 0]
