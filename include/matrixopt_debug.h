@@ -20,7 +20,8 @@ extern "C" {
  * bytes from the workspace base).  Orientation: m = min(rows, cols),
  * n = max(rows, cols), transposed = rows > cols.
  *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong (ldx),
- *              x_master = fp32 m x n (ldx), gram = bf16 m x m (lda),
+ *              x_master = fp32 master of X in a private tile-native layout
+ *              (ceil(m/128)*128 x ceil(n/256)*256 floats), gram = bf16 m x m (lda),
  *              poly = bf16 m x m (lda).
  *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong (x_master = 0),
  *              gram, poly = fp32 m x m.

@@ -145,6 +145,11 @@ struct MatBufs {
 };
 
 // Counts of tiles per phase for one matrix.
+// fp32 master of X: whole 128 x 256 blocks (a tile-native layout, padded).
+size_t master_bytes(int64_t m, int64_t n) {
+    return static_cast<size_t>(ceil_div(m, 128) * 128) * static_cast<size_t>(ceil_div(n, 256) * 256) * 4;
+}
+
 // Rows of one tensor-core output tile: 128 for a single CTA, 256 for a CTA pair.
 int64_t tile_rows(bool pair) { return pair ? 2 * kTcBM : kTcBM; }
 
@@ -237,7 +242,7 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
         b.x_op[1] = off; off = align_up(off + xbytes, kBufAlign);
         if (precision == MO_NS_BF16) {
             b.x_master = off;
-            off = align_up(off + static_cast<size_t>(s.m) * s.ldx * 4, kBufAlign);
+            off = align_up(off + master_bytes(s.m, s.n), kBufAlign);
         } else {
             b.x_master = 0;
         }
@@ -432,6 +437,7 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
         d.x_op[0] = base + b.x_op[0];
         d.x_op[1] = base + b.x_op[1];
         d.x_master = o.precision == MO_NS_BF16 ? reinterpret_cast<float*>(base + b.x_master) : nullptr;
+        d.master_jb = static_cast<int32_t>(ceil_div(s.n, 256));
         d.gram = base + b.gram;
         d.poly = base + b.poly;
         d.scales = reinterpret_cast<float*>(base + L.scales) + kScaleStride * i;

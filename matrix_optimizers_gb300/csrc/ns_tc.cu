@@ -177,6 +177,29 @@ __device__ __forceinline__ void store32_stream(float* p, int64_t off, int nv, co
             if (k < nv) __stcs(p + off + k, v[k]);
     }
 }
+// fp32 master of X in a tile-native layout: blocks of 128 rows x 256
+// columns (block (i / 128, j / 256) at float offset 32768 x (i / 128 x
+// master_jb + j / 256)), each stored as [column / 4][row][column % 4].  The
+// 32 lanes of an epilogue warp hold 32 consecutive rows, so each float4 they
+// move is one contiguous 512-byte run.  The layout is private to the NS path.
+__device__ __forceinline__ float4* master_ptr(const MatDesc& md, int i, int j0) {
+    const int64_t blk = static_cast<int64_t>(i >> 7) * md.master_jb + (j0 >> 8);
+    return reinterpret_cast<float4*>(md.x_master) + blk * (128 * 64) + ((j0 & 255) >> 2) * 128 + (i & 127);
+}
+__device__ __forceinline__ void master_load32(const MatDesc& md, int i, int j0, float (&v)[32]) {
+    const float4* s = master_ptr(md, i, j0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const float4 x = __ldcs(s + q * 128);
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    }
+}
+__device__ __forceinline__ void master_store32(const MatDesc& md, int i, int j0, const float (&v)[32]) {
+    float4* d = master_ptr(md, i, j0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) __stcs(d + q * 128, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+}
+
 // bf16 Gram entries written by other CTAs of the same launch: read at L2
 // (ld.global.cg), never from a non-coherent cache.
 __device__ __forceinline__ void load32_bf16_l2(const bf16* p, int64_t off, int nv, float (&v)[32]) {
@@ -307,15 +330,19 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
     } else {
-        load32_stream(md.x_master, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
+        if (row_ok) {
+            master_load32(md, i, j0, x);      // whole 32 columns: the layout pads to 256
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[k] = 0.f;
+        }
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
     }
     if (step + 1 < p.steps) {
         if (!row_ok) return;
-        const int64_t off = static_cast<int64_t>(i) * md.ldx + j0;
-        store32_stream(md.x_master, off, nv, x);
-        store32(md.x_op[(step + 1) & 1], MO_BF16, off, nv, x);
+        master_store32(md, i, j0, x);
+        store32(md.x_op[(step + 1) & 1], MO_BF16, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
         return;
     }
     if (md.sign_words != nullptr) {

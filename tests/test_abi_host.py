@@ -159,7 +159,8 @@ def test_debug_view_offsets_are_disjoint():
         assert v.transposed == (1 if i == 1 else 0)
         assert v.ldx % 64 == 0 and v.lda % 64 == 0
         xb = v.m * v.ldx * 2
-        spans += [(v.x_op[0], xb), (v.x_op[1], xb), (v.x_master, v.m * v.ldx * 4),
+        master = -(-v.m // 128) * 128 * (-(-v.n // 256) * 256) * 4       # tile-native, padded
+        spans += [(v.x_op[0], xb), (v.x_op[1], xb), (v.x_master, master),
                   (v.gram, v.m * v.lda * 2), (v.poly, v.m * v.lda * 2)]
     spans.sort()
     for (a, la), (b, _) in zip(spans, spans[1:]):
