@@ -100,22 +100,88 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float* v) {
     return u;
 }
 
+// 256-bit global accesses (sm_100 and later): one whole 32-byte sector per
+// lane and instruction.  `p` must be 32-byte aligned.
+__device__ __forceinline__ void ld_v8(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void ld_v8_cs(const void* p, uint32_t (&w)[8]) {     // evict-first
+    asm volatile("ld.global.cs.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void ld_v8_cg(const void* p, uint32_t (&w)[8]) {     // at L2
+    asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+__device__ __forceinline__ void st_v8_cs(void* p, const uint32_t (&w)[8]) {     // evict-first
+    asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+__device__ __forceinline__ bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31) == 0; }
+
+__device__ __forceinline__ void unpack_bf16x16(const uint32_t (&w)[8], float* v) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        v[2 * q] = __uint_as_float(w[q] << 16);
+        v[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+}
+__device__ __forceinline__ void pack_bf16x16(const float* v, uint32_t (&w)[8]) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+        w[q] = *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
 // 32 consecutive elements starting at p[off]; `nv` of them valid.  A full
-// group is read with 16-byte vector loads (offsets are 32-element aligned
-// and leading dimensions 16-byte multiples).
+// group moves as 32-byte accesses where the row segment is 32-byte aligned
+// (16-byte vectors otherwise; offsets are 32-element aligned and leading
+// dimensions 16-byte multiples).
 __device__ __forceinline__ void load32(const void* p, int dt, int64_t off, int nv, float (&v)[32]) {
     if (nv == 32) {
         if (dt == MO_F32) {
-            const float4* s = reinterpret_cast<const float4*>(static_cast<const float*>(p) + off);
+            const float* s = static_cast<const float*>(p) + off;
+            if (aligned32(s)) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 x = s[q];
-                v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[8];
+                    ld_v8(s + 8 * q, w);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[8 * q + k] = __uint_as_float(w[k]);
+                }
+            } else {
+                const float4* s4 = reinterpret_cast<const float4*>(s);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 x = s4[q];
+                    v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+                }
             }
         } else {
-            const uint4* s = reinterpret_cast<const uint4*>(static_cast<const bf16*>(p) + off);
+            const bf16* s = static_cast<const bf16*>(p) + off;
+            if (aligned32(s)) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) unpack_bf16x8(s[q], &v[8 * q]);
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t w[8];
+                    ld_v8(s + 16 * q, w);
+                    unpack_bf16x16(w, &v[16 * q]);
+                }
+            } else {
+                const uint4* s4 = reinterpret_cast<const uint4*>(s);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) unpack_bf16x8(s4[q], &v[8 * q]);
+            }
         }
     } else {
 #pragma unroll
@@ -131,13 +197,34 @@ __device__ __forceinline__ void load32(const void* p, int dt, int64_t off, int n
 __device__ __forceinline__ void store32(void* p, int dt, int64_t off, int nv, const float (&v)[32]) {
     if (nv == 32) {
         if (dt == MO_F32) {
-            float4* d = reinterpret_cast<float4*>(static_cast<float*>(p) + off);
+            float* d = static_cast<float*>(p) + off;
+            if (aligned32(d)) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t w[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(v[8 * q + k]);
+                    st_v8(d + 8 * q, w);
+                }
+            } else {
+                float4* d4 = reinterpret_cast<float4*>(d);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
         } else {
-            uint4* d = reinterpret_cast<uint4*>(static_cast<bf16*>(p) + off);
+            bf16* d = static_cast<bf16*>(p) + off;
+            if (aligned32(d)) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) d[q] = pack_bf16x8(&v[8 * q]);
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t w[8];
+                    pack_bf16x16(&v[16 * q], w);
+                    st_v8(d + 16 * q, w);
+                }
+            } else {
+                uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) d4[q] = pack_bf16x8(&v[8 * q]);
+            }
         }
     } else {
 #pragma unroll
@@ -151,62 +238,47 @@ __device__ __forceinline__ void store32(void* p, int dt, int64_t off, int nv, co
         }
     }
 }
-// fp32 master of X: touched once per phase, so read and written with
-// evict-first hints to leave L2 to the GEMM operands.
-__device__ __forceinline__ void load32_stream(const float* p, int64_t off, int nv, float (&v)[32]) {
-    if (nv == 32) {
-        const float4* s = reinterpret_cast<const float4*>(p + off);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 x = __ldcs(s + q);
-            v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = k < nv ? __ldcs(p + off + k) : 0.f;
-    }
-}
-__device__ __forceinline__ void store32_stream(float* p, int64_t off, int nv, const float (&v)[32]) {
-    if (nv == 32) {
-        float4* d = reinterpret_cast<float4*>(p + off);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) __stcs(d + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
-    } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-            if (k < nv) __stcs(p + off + k, v[k]);
-    }
-}
 // fp32 master of X in a tile-native layout: blocks of 128 rows x 256
 // columns (block (i / 128, j / 256) at float offset 32768 x (i / 128 x
-// master_jb + j / 256)), each stored as [column / 4][row][column % 4].  The
-// 32 lanes of an epilogue warp hold 32 consecutive rows, so each float4 they
-// move is one contiguous 512-byte run.  The layout is private to the NS path.
-__device__ __forceinline__ float4* master_ptr(const MatDesc& md, int i, int j0) {
+// master_jb + j / 256)), each stored as [column / 8][row][column % 8].  The
+// 32 lanes of an epilogue warp hold 32 consecutive rows, so each 32-byte
+// access they make is one contiguous 1 KB run.  It is touched once per step,
+// with evict-first hints.  The layout is private to the NS path.
+__device__ __forceinline__ float* master_ptr(const MatDesc& md, int i, int j0) {
     const int64_t blk = static_cast<int64_t>(i >> 7) * md.master_jb + (j0 >> 8);
-    return reinterpret_cast<float4*>(md.x_master) + blk * (128 * 64) + ((j0 & 255) >> 2) * 128 + (i & 127);
+    return md.x_master + blk * (128 * 256) + (((j0 & 255) >> 3) * 128 + (i & 127)) * 8;
 }
 __device__ __forceinline__ void master_load32(const MatDesc& md, int i, int j0, float (&v)[32]) {
-    const float4* s = master_ptr(md, i, j0);
+    const float* s = master_ptr(md, i, j0);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const float4 x = __ldcs(s + q * 128);
-        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[8];
+        ld_v8_cs(s + q * 128 * 8, w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[8 * q + k] = __uint_as_float(w[k]);
     }
 }
 __device__ __forceinline__ void master_store32(const MatDesc& md, int i, int j0, const float (&v)[32]) {
-    float4* d = master_ptr(md, i, j0);
+    float* d = master_ptr(md, i, j0);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) __stcs(d + q * 128, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    for (int q = 0; q < 4; ++q) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(v[8 * q + k]);
+        st_v8_cs(d + q * 128 * 8, w);
+    }
 }
 
 // bf16 Gram entries written by other CTAs of the same launch: read at L2
 // (ld.global.cg), never from a non-coherent cache.
 __device__ __forceinline__ void load32_bf16_l2(const bf16* p, int64_t off, int nv, float (&v)[32]) {
     if (nv == 32) {
-        const uint4* s = reinterpret_cast<const uint4*>(p + off);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) unpack_bf16x8(__ldcg(s + q), &v[8 * q]);
+        for (int q = 0; q < 2; ++q) {
+            uint32_t w[8];
+            ld_v8_cg(p + off + 16 * q, w);        // lda is a multiple of 64: 32-byte aligned
+            unpack_bf16x16(w, &v[16 * q]);
+        }
     } else {
         const unsigned short* h = reinterpret_cast<const unsigned short*>(p + off);
 #pragma unroll
