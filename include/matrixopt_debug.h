@@ -19,9 +19,9 @@ extern "C" {
  * ns_orthogonalize / muon_step_batched use for these shapes (offsets are in
  * bytes from the workspace base).  Orientation: m = min(rows, cols),
  * n = max(rows, cols), transposed = rows > cols.
- *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong (ldx),
- *              x_master = fp32 master of X in a private tile-native layout
- *              (ceil(m/128)*128 x ceil(n/256)*256 floats), gram = bf16 m x m (lda),
+ *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong (ldx; X
+ *              is kept in bf16 between steps, x_master = 0),
+ *              gram = bf16 m x m (lda),
  *              poly = bf16 m x m (lda).
  *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong (x_master = 0),
  *              gram, poly = fp32 m x m.

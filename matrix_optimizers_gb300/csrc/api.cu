@@ -143,15 +143,10 @@ Shape oriented(int64_t rows, int64_t cols) {
 }
 
 struct MatBufs {
-    size_t x_op[2], x_master, gram, poly;
+    size_t x_op[2], gram, poly;
 };
 
 // Counts of tiles per phase for one matrix.
-// fp32 master of X: whole 128 x 256 blocks (a tile-native layout, padded).
-size_t master_bytes(int64_t m, int64_t n) {
-    return static_cast<size_t>(ceil_div(m, 128) * 128) * static_cast<size_t>(ceil_div(n, 256) * 256) * 4;
-}
-
 // Rows of one tensor-core output tile: 128 for a single CTA, 256 for a CTA pair.
 int64_t tile_rows(bool pair) { return pair ? 2 * kTcBM : kTcBM; }
 
@@ -242,12 +237,6 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
         MatBufs& b = L.buf[i];
         b.x_op[0] = off; off = align_up(off + xbytes, kBufAlign);
         b.x_op[1] = off; off = align_up(off + xbytes, kBufAlign);
-        if (precision == MO_NS_BF16) {
-            b.x_master = off;
-            off = align_up(off + master_bytes(s.m, s.n), kBufAlign);
-        } else {
-            b.x_master = 0;
-        }
         b.gram = off; off = align_up(off + abytes, kBufAlign);
         b.poly = off; off = align_up(off + abytes, kBufAlign);
     }
@@ -438,8 +427,6 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
         d.sign_words = j.words;
         d.x_op[0] = base + b.x_op[0];
         d.x_op[1] = base + b.x_op[1];
-        d.x_master = o.precision == MO_NS_BF16 ? reinterpret_cast<float*>(base + b.x_master) : nullptr;
-        d.master_jb = static_cast<int32_t>(ceil_div(s.n, 256));
         d.gram = base + b.gram;
         d.poly = base + b.poly;
         d.scales = reinterpret_cast<float*>(base + L.scales) + kScaleStride * i;
@@ -1078,7 +1065,7 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
     view->precision = precision;
     view->x_op[0] = static_cast<int64_t>(b.x_op[0]);
     view->x_op[1] = static_cast<int64_t>(b.x_op[1]);
-    view->x_master = static_cast<int64_t>(b.x_master);
+    view->x_master = 0;                  // X is kept in bf16 only (the operand pair)
     view->gram = static_cast<int64_t>(b.gram);
     view->poly = static_cast<int64_t>(b.poly);
     view->deps = static_cast<int64_t>(L.deps + 4 * sizeof(int) * static_cast<size_t>(active));

@@ -53,8 +53,6 @@ struct MatDesc {
     void* out;                 // NS output target or null
     uint32_t* sign_words;      // fused sign + 1-bit pack target of the output, or null
     void* x_op[2];             // NS operand ping-pong (bf16 or fp32), m x ldx
-    float* x_master;           // fp32 master of X (bf16 mode), tile-native 128 x 256 blocks
-    int32_t master_jb;         // 256-column blocks of the master (ceil(n / 256))
     void* gram;                // m x lda  (A = X X^T)
     void* poly;                // m x lda  (B = b A + c A^2)
     const CUtensorMap* tm_x[2];

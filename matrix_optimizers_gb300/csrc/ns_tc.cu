@@ -238,37 +238,6 @@ __device__ __forceinline__ void store32(void* p, int dt, int64_t off, int nv, co
         }
     }
 }
-// fp32 master of X in a tile-native layout: blocks of 128 rows x 256
-// columns (block (i / 128, j / 256) at float offset 32768 x (i / 128 x
-// master_jb + j / 256)), each stored as [column / 8][row][column % 8].  The
-// 32 lanes of an epilogue warp hold 32 consecutive rows, so each 32-byte
-// access they make is one contiguous 1 KB run.  It is touched once per step,
-// with evict-first hints.  The layout is private to the NS path.
-__device__ __forceinline__ float* master_ptr(const MatDesc& md, int i, int j0) {
-    const int64_t blk = static_cast<int64_t>(i >> 7) * md.master_jb + (j0 >> 8);
-    return md.x_master + blk * (128 * 256) + (((j0 & 255) >> 3) * 128 + (i & 127)) * 8;
-}
-__device__ __forceinline__ void master_load32(const MatDesc& md, int i, int j0, float (&v)[32]) {
-    const float* s = master_ptr(md, i, j0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t w[8];
-        ld_v8_cs(s + q * 128 * 8, w);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[8 * q + k] = __uint_as_float(w[k]);
-    }
-}
-__device__ __forceinline__ void master_store32(const MatDesc& md, int i, int j0, const float (&v)[32]) {
-    float* d = master_ptr(md, i, j0);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(v[8 * q + k]);
-        st_v8_cs(d + q * 128 * 8, w);
-    }
-}
-
 // bf16 Gram entries written by other CTAs of the same launch: read at L2
 // (ld.global.cg), never from a non-coherent cache.
 __device__ __forceinline__ void load32_bf16_l2(const bf16* p, int64_t off, int nv, float (&v)[32]) {
@@ -396,24 +365,20 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     if (j0 >= n) return;
     const int nv = row_ok ? min(32, n - j0) : 0;
     float x[32];
+    // The aX term uses this step's bf16 operand, the same values the products
+    // read: bf16(M) (unscaled, from the momentum kernel) at step 0, else X_t,
+    // written by this thread one step earlier.
+    load32(md.x_op[step & 1], MO_BF16, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
     if (step == 0) {
-        user_load32(md, md.src, md.src_dtype, i, j0, nv, x);
         const float inv_s = md.scales[0] * md.scales[4];      // 1/||M||_F (x 1/sigma_hat when spectral)
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
     } else {
-        if (row_ok) {
-            master_load32(md, i, j0, x);      // whole 32 columns: the layout pads to 256
-        } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) x[k] = 0.f;
-        }
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
     }
     if (step + 1 < p.steps) {
         if (!row_ok) return;
-        master_store32(md, i, j0, x);
         store32(md.x_op[(step + 1) & 1], MO_BF16, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
         return;
     }

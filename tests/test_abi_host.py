@@ -82,8 +82,8 @@ def test_workspace_bytes_host_only():
             B.mo_matrix(3072, 768, 768, 0, 0, 0, 0, 16, 16, 16)]
     cfg = B.make_cfg()
     ws = B.mo_workspace_bytes(mats, cfg)
-    # both orient to 768 x 3072: operands 2 x bf16 X + fp32 master + 2 x 768^2 bf16 each
-    per = 768 * 3072 * (2 + 2 + 4) + 2 * 768 * 768 * 2
+    # both orient to 768 x 3072: operands 2 x bf16 X + 2 x 768^2 bf16 each
+    per = 768 * 3072 * (2 + 2) + 2 * 768 * 768 * 2
     assert 2 * per <= ws < 2 * per + (1 << 20)
     assert ws == B.ns_workspace_bytes([(768, 3072), (3072, 768)])
     cfg32 = B.make_cfg(precision=B.MO_NS_FP32)
@@ -159,8 +159,8 @@ def test_debug_view_offsets_are_disjoint():
         assert v.transposed == (1 if i == 1 else 0)
         assert v.ldx % 64 == 0 and v.lda % 64 == 0
         xb = v.m * v.ldx * 2
-        master = -(-v.m // 128) * 128 * (-(-v.n // 256) * 256) * 4       # tile-native, padded
-        spans += [(v.x_op[0], xb), (v.x_op[1], xb), (v.x_master, master),
+        assert v.x_master == 0                                # X stays in bf16 between steps
+        spans += [(v.x_op[0], xb), (v.x_op[1], xb),
                   (v.gram, v.m * v.lda * 2), (v.poly, v.m * v.lda * 2)]
     spans.sort()
     for (a, la), (b, _) in zip(spans, spans[1:]):

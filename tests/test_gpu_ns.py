@@ -54,7 +54,7 @@ def test_phases_individually(shape):
     want_poly = Bc * gram + C * gram @ gram
     assert rel_fro(poly, want_poly) < 4e-3
     assert np.array_equal(poly, poly.T)
-    want_x1 = (A * Xo.astype(np.float32) + poly @ Xb) / s
+    want_x1 = (A * Xb + poly @ Xb) / s                                   # aX from the bf16 operand too
     got = outs[0].T if v.transposed else outs[0]
     assert rel_fro(got, want_x1) < 1e-5
 
