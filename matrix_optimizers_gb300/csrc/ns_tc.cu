@@ -2,8 +2,8 @@
 //
 // Three phases per iteration, each a grouped GEMM over every matrix of the batch:
 //   kGram   A = s * X X^T          (X: m x n bf16, K = n; s = 1/||M||_F^2 at step 0)
-//   kPoly   B = b*A + c * A A      (K = m; A is symmetric so A A = A A^T)
-//   kApply  X' = a*X + B X         (K = m; step 0: X' = (a*M + B Xb)/||M||_F)
+//   kPoly   B = a*I + b*A + c * A A   (K = m; A is symmetric so A A = A A^T)
+//   kApply  X' = B X               (K = m; step 0: X' = B Xb / ||M||_F, Xb = bf16(M))
 //           the last step writes W <- W - lr*wd*W - lr*scale*X' (or the output)
 // kGram and kPoly compute only the 128 x 256 tiles that meet the upper
 // triangle (j >= i) and store each upper element at (i, j) and (j, i).
@@ -302,11 +302,13 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
     } else {
         float a[32];
         load32_bf16_l2(static_cast<const bf16*>(md.gram), static_cast<int64_t>(i) * md.lda + j0, nv, a);
-        // step 0 folds the spectral scale into the coefficients (1 otherwise)
+        // step 0 folds the spectral scale into the coefficients (1 otherwise);
+        // the diagonal also takes a: B = bA + cA^2 + aI, so that the apply
+        // phase is the plain product X' = B X
         const float bs = step == 0 ? p.b * md.scales[2] : p.b;
         const float cs = step == 0 ? p.c * md.scales[3] : p.c;
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = fmaf(cs, v[k], bs * a[k]);
+        for (int k = 0; k < 32; ++k) v[k] = fmaf(cs, v[k], bs * a[k]) + (j0 + k == i ? p.a : 0.f);
     }
     const int64_t row = static_cast<int64_t>(i) * md.lda;
     if (j0 >= i) {
@@ -365,18 +367,11 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     if (j0 >= n) return;
     const int nv = row_ok ? min(32, n - j0) : 0;
     float x[32];
-    // The aX term uses this step's bf16 operand, the same values the products
-    // read: bf16(M) (unscaled, from the momentum kernel) at step 0, else X_t,
-    // written by this thread one step earlier.
-    load32(md.x_op[step & 1], MO_BF16, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
-    if (step == 0) {
-        const float inv_s = md.scales[0] * md.scales[4];      // 1/||M||_F (x 1/sigma_hat when spectral)
+    // X' = (aI + bA + cA^2) X is the accumulator (the polynomial phase put a
+    // on B's diagonal); step 0 multiplied the unscaled bf16(M), so it scales.
+    const float scale = step == 0 ? md.scales[0] * md.scales[4] : 1.f;   // 1/||M||_F (x 1/sigma_hat)
 #pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = inv_s * fmaf(p.a, x[k], v[k]);
-    } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = fmaf(p.a, x[k], v[k]);
-    }
+    for (int k = 0; k < 32; ++k) x[k] = scale * v[k];
     if (step + 1 < p.steps) {
         if (!row_ok) return;
         store32(md.x_op[(step + 1) & 1], MO_BF16, static_cast<int64_t>(i) * md.ldx + j0, nv, x);

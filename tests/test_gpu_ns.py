@@ -51,10 +51,10 @@ def test_phases_individually(shape):
     assert rel_fro(gram, want_gram) < 4e-3                                # bf16 storage of A
     assert np.array_equal(gram, gram.T)                                   # mirrored exactly
     poly = to_np(ws_view(ws, v.poly, (m, m), torch.bfloat16, v.lda))
-    want_poly = Bc * gram + C * gram @ gram
+    want_poly = A * np.eye(m) + Bc * gram + C * gram @ gram              # a folded onto the diagonal
     assert rel_fro(poly, want_poly) < 4e-3
     assert np.array_equal(poly, poly.T)
-    want_x1 = (A * Xb + poly @ Xb) / s                                   # aX from the bf16 operand too
+    want_x1 = poly @ Xb / s                                               # X1 = (aI + bA + cA^2) X0
     got = outs[0].T if v.transposed else outs[0]
     assert rel_fro(got, want_x1) < 1e-5
 
