@@ -40,8 +40,8 @@ METRIC = "Muon step matrices/s and NS TFLOP/s (fraction of bf16 peak); vote GB/s
 # shape the kernel and its schedule hash to the value recorded with it.
 PROFILED_TRAFFIC = {
     ("llama7b_owner0", "fused"): {
-        "bytes_per_launch": 68.17e9 + 32.05e9,
-        "sources_sha256": "c84948847abe30e57c1770344d44a5e1e7eaf17acd352dc97c6f1e670286a25b",
+        "bytes_per_launch": 45.89e9 + 19.09e9,
+        "sources_sha256": "4ae24ab97f8f8a86d52ac55555b0bc9ab73c03a5a84a7a34ad36f756f6f4a2d2",
         "profile": "profiles/launches_llama7b_owner0.md",
     },
 }
@@ -49,10 +49,10 @@ TRAFFIC_SOURCES = ["matrix_optimizers_gb300/csrc/ns_tc.cu", "matrix_optimizers_g
                    "matrix_optimizers_gb300/csrc/internal.h", "matrix_optimizers_gb300/csrc/api.cu"]
 
 
-def _profiled_traffic(workload, ns_launch, max_matrices):
+def _profiled_traffic(workload, ns_launch, max_matrices, ns_tiles):
     import hashlib
     rec = PROFILED_TRAFFIC.get((workload, ns_launch))
-    if rec is None or max_matrices:
+    if rec is None or max_matrices or ns_tiles not in (None, "single"):
         return None, None
     h = hashlib.sha256()
     root = os.path.dirname(os.path.abspath(__file__))
@@ -323,7 +323,7 @@ def run_gb300(args, rank, world, local_rank, dist):
     ns_tflops_kernel = flops_step * args.steps / (ns_ms * 1e-3) / 1e12 if ns_ms > 0 else None
     ns_tflops_step = flops_step / (ms_step * 1e-3) / 1e12
     sustained = peaks["bf16_tflops_sustained"]
-    traffic, traffic_src = _profiled_traffic(args.workload, args.ns_launch, args.max_matrices)
+    traffic, traffic_src = _profiled_traffic(args.workload, args.ns_launch, args.max_matrices, args.ns_tiles)
     all_ms = sum(v[1] for v in by_kind.values())
     result = {
         "metric": METRIC, "value": total_mats / (ms_step * 1e-3), "unit": "matrices/s",

@@ -59,10 +59,10 @@ int mo_debug_sm_count(void);
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
 /* Chooses the tile geometry of the bf16 tensor-core Newton-Schulz kernel:
- * on = 1 (the default) runs 256 x 256 tiles on CTA pairs (clusters of 2,
- * tcgen05 cta_group::2: each CTA loads 128 rows of A and 128 columns of B)
- * when the device can co-schedule such clusters; on = 0 runs 128 x 256 tiles
- * on single CTAs.  Results are identical.  Returns the previous setting, or
+ * on = 1 runs 256 x 256 tiles on CTA pairs (clusters of 2, tcgen05
+ * cta_group::2: each CTA loads 128 rows of A and 128 columns of B) when the
+ * device can co-schedule such clusters; on = 0 (the default) runs 128 x 256
+ * tiles on single CTAs.  Results are identical.  Returns the previous setting, or
  * MO_ERR_INVALID_ARG for a value other than 0 / 1.  Process-wide. */
 int mo_debug_set_ns_pair(int on);
 

@@ -94,11 +94,12 @@ std::atomic<int> g_ns_fused{3};
 // next phase fill the tail) wins; above it the grid-wide ordering keeps every
 // CTA on the same few matrices, which measured faster through L2 reuse.
 constexpr int64_t kPerMatrixDepsMaxSymTilesPerCta = 16;
-// 1 (default): the tensor-core kernel runs 256 x 256 tiles on CTA pairs
-// (cta_group::2) when the device can co-schedule 2-CTA clusters; 0: 128 x 256
-// tiles per CTA.  The pair form measured 1-2% faster on the large workloads
-// and equal on the small ones.
-std::atomic<int> g_ns_pair{1};
+// 1: the tensor-core kernel runs 256 x 256 tiles on CTA pairs (cta_group::2)
+// when the device can co-schedule 2-CTA clusters; 0 (default): 128 x 256
+// tiles per CTA.  The two measured within about 1% of each other on every
+// workload; the single-CTA form is the default because its fused
+// (cooperative) launch can also be captured by the profiler.
+std::atomic<int> g_ns_pair{0};
 
 // Co-resident CTAs of the tensor-core kernel per device ordinal, queried once.
 std::mutex g_cap_mu;
