@@ -8,9 +8,34 @@
 //   adamw          vectorised AdamW on the flat float32 tail.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <atomic>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mo {
+
+namespace {
+// Resident blocks per SM of `kernel` at `threads` threads (queried once per
+// kernel and device); 1 if the query fails.  Grids of the one-pass
+// streaming kernels are sized to a single resident wave.
+template <typename K>
+int resident_blocks_per_sm(K kernel, int threads) {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    int v = cache[dev & 63].load();
+    if (v > 0) return v;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    cache[dev & 63].store(n);
+    return n;
+}
+}  // namespace
 
 using bf16 = __nv_bfloat16;
 
@@ -358,7 +383,9 @@ cudaError_t launch_sign_pack_batched(const void* const* U, uint32_t* const* word
         }
         const int64_t warps_needed = (rows * cols / 8 + 127) / 128;
         const int64_t blocks = (warps_needed + 7) / 8;
-        int64_t cap = device_sm_count() * 8LL / M;
+        const int per_sm = dtype == MO_F32 ? resident_blocks_per_sm(sign_pack_vec_kernel<float>, 256)
+                                           : resident_blocks_per_sm(sign_pack_vec_kernel<bf16>, 256);
+        int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm / M;     // one resident wave
         if (cap < 1) cap = 1;
         const dim3 grid(static_cast<unsigned>(blocks < cap ? blocks : cap), static_cast<unsigned>(M));
         if (dtype == MO_F32)
@@ -523,30 +550,148 @@ __global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_const
     const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     for (int64_t base = warp * 32; base < nwords; base += nwarps * 32) {
-        // W loads first, so they are in flight with the word loads below
-        int64_t e = base * 32 + 4 * lane;
-        int64_t r = e / cols, c = e - r * cols;
-        int64_t idx[8];
+        // W loads first, so they are in flight with the word loads below; the
+        // store pass walks the same positions again rather than keeping them
+        const int64_t e = base * 32 + 4 * lane;
+        const int64_t r0 = e / cols, c0 = e - r0 * cols;
         V val[8];
+        {
+            int64_t r = r0, c = c0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            idx[q] = e + 128 * q < numel ? r * ld + c : -1;
-            if (idx[q] >= 0) val[q] = *reinterpret_cast<const V*>(W + idx[q]);
-            c += 128;
-            while (c >= cols) { c -= cols; ++r; }
+            for (int q = 0; q < 8; ++q) {
+                if (e + 128 * q < numel) val[q] = *reinterpret_cast<const V*>(W + r * ld + c);
+                c += 128;
+                while (c >= cols) { c -= cols; ++r; }
+            }
         }
         const uint32_t plus = base + lane < nwords ? vote_word(ptrs, M, nbits, thr, base + lane) : 0u;
+        int64_t r = r0, c = c0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const uint32_t vw = __shfl_sync(0xffffffffu, plus, 4 * q + (lane >> 3));
             const uint32_t bits = vw >> (4 * (lane & 7));
-            if (idx[q] >= 0) {
+            if (e + 128 * q < numel) {
                 float x[4];
                 Vec4<T>::unpack(val[q], x);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) x[k] = ((bits >> k) & 1u) ? (x[k] - lr) : (x[k] + lr);
-                *reinterpret_cast<V*>(W + idx[q]) = Vec4<T>::pack(x);
+                *reinterpret_cast<V*>(W + r * ld + c) = Vec4<T>::pack(x);
             }
+            c += 128;
+            while (c >= cols) { c -= cols; ++r; }
+        }
+    }
+}
+
+// ------------------------------------------------- vote + update, bulk path
+// For a contiguous W (ld == cols) whose element count is a multiple of
+// kVoteChunk, with up to kBulkVoters workers: each block streams chunks of
+// kVoteChunk elements through shared memory, two chunks in flight.  A chunk's
+// W and its kVoteChunk/32 words of every worker arrive by bulk copies on one
+// mbarrier; the 256 threads count one word each, then update the chunk in
+// shared memory with consecutive threads on consecutive elements; one bulk
+// store writes it back.  Same arithmetic as vote_update_vec_kernel.
+constexpr int kVoteChunk = 8192;
+constexpr int kVoteChunkWords = kVoteChunk / 32;
+constexpr int kBulkVoters = 16;
+
+__device__ __forceinline__ bool wait_phase_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) vote_update_bulk_kernel(const __grid_constant__ VotePtrs ptrs, int M,
+                                                               int nbits, uint32_t thr, T* __restrict__ W, float lr,
+                                                               int64_t nchunks) {
+    extern __shared__ __align__(128) uint8_t vsm[];
+    __shared__ __align__(8) uint64_t full[2];
+    __shared__ uint32_t vote[kVoteChunkWords];
+    constexpr uint32_t kWBytes = kVoteChunk * sizeof(T);
+    const uint32_t stage_bytes = kWBytes + static_cast<uint32_t>(M) * kVoteChunkWords * 4;
+    const int t = threadIdx.x;
+    if (t == 0) {
+        mbar_init(smem_u32(&full[0]), 1);
+        mbar_init(smem_u32(&full[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t c, int st) {                 // thread 0
+        uint8_t* base = vsm + st * stage_bytes;
+        const uint32_t bar = smem_u32(&full[st]);
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_load(smem_u32(base), W + c * kVoteChunk, kWBytes, bar);
+        for (int m = 0; m < M; ++m)
+            bulk_load(smem_u32(base + kWBytes + m * kVoteChunkWords * 4), ptrs.w[m] + c * kVoteChunkWords,
+                      kVoteChunkWords * 4, bar);
+    };
+    const int64_t c0 = blockIdx.x;
+    if (t == 0) {
+        if (c0 < nchunks) issue(c0, 0);
+        if (c0 + gridDim.x < nchunks) issue(c0 + gridDim.x, 1);
+    }
+    int k = 0;
+    bool ok = true;
+    for (int64_t c = c0; c < nchunks; c += gridDim.x, ++k) {
+        const int st = k & 1;
+        ok = wait_phase_bounded(smem_u32(&full[st]), (k >> 1) & 1);
+        if (!__syncthreads_and(ok)) break;                 // never expected: a bounded give-up
+        uint8_t* base = vsm + st * stage_bytes;
+        const uint32_t* wd = reinterpret_cast<const uint32_t*>(base + kWBytes);
+        // bit-sliced count of +1 votes of word t over the M workers
+        uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int m = 0; m < M; ++m) {
+            uint32_t x = wd[m * kVoteChunkWords + t];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j < nbits) {
+                    const uint32_t carry = cnt[j] & x;
+                    cnt[j] ^= x;
+                    x = carry;
+                }
+            }
+        }
+        uint32_t gt = 0u, eq = 0xffffffffu;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            if (j < nbits) {
+                if ((thr >> j) & 1u) {
+                    eq &= cnt[j];
+                } else {
+                    gt |= eq & cnt[j];
+                    eq &= ~cnt[j];
+                }
+            }
+        }
+        vote[t] = gt | eq;
+        __syncthreads();
+        T* w = reinterpret_cast<T*>(base);
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const int e = t + 256 * j;
+            const float x = static_cast<float>(w[e]);
+            w[e] = static_cast<T>(((vote[e >> 5] >> (e & 31)) & 1u) ? (x - lr) : (x + lr));
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0) {
+            bulk_store(W + c * kVoteChunk, smem_u32(base), kWBytes);
+            bulk_commit();
+            const int64_t cn = c + 2 * static_cast<int64_t>(gridDim.x);
+            if (cn < nchunks) {
+                bulk_wait_read_all();                      // the stage is free once the store has read it
+                issue(cn, st);
+            }
+        }
+    }
+    if (t == 0) {
+        bulk_wait_all();
+        if (!ok) {
+            // let copies still landing in this block's shared memory finish
+            for (int s2 = 0; s2 < 2; ++s2) (void)wait_phase_bounded(smem_u32(&full[s2]), (k >> 1) & 1);
         }
     }
 }
@@ -562,10 +707,51 @@ cudaError_t launch_sign_vote_update(const uint32_t* const* words, int M, int64_t
     const uint32_t thr = static_cast<uint32_t>((M + 1) / 2);
     const int64_t warps_needed = (nwords + 31) / 32;
     const int64_t blocks = (warps_needed + 7) / 8;
-    const int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
+    int grid = static_cast<int>(blocks < device_sm_count() * 16LL ? blocks : device_sm_count() * 16LL);
     const size_t vbytes = w_dtype == MO_F32 ? 16 : 8;
     const bool vec = cols % 4 == 0 && ld % 4 == 0 && (reinterpret_cast<uintptr_t>(W) % vbytes) == 0;
+    const int64_t numel = rows * cols;
+    bool bulk = ld == cols && numel % kVoteChunk == 0 && M <= kBulkVoters && (reinterpret_cast<uintptr_t>(W) & 15u) == 0;
+    for (int m = 0; m < M && bulk; ++m) bulk = (reinterpret_cast<uintptr_t>(words[m]) & 15u) == 0;
+    if (bulk) {
+        const int esz = w_dtype == MO_F32 ? 4 : 2;
+        const int smem = 2 * (kVoteChunk * esz + M * kVoteChunkWords * 4);
+        static std::atomic<uint64_t> attr_set{0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = uint64_t(1) << (dev & 63);
+        if (!(attr_set.load() & bit)) {
+            const int max_smem = 2 * (kVoteChunk * 4 + kBulkVoters * kVoteChunkWords * 4);
+            e = cudaFuncSetAttribute(vote_update_bulk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     max_smem);
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(vote_update_bulk_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     max_smem);
+            if (e != cudaSuccess) return e;
+            attr_set.fetch_or(bit);
+        }
+        const int64_t nchunks = numel / kVoteChunk;
+        int per_sm = 0;
+        if (w_dtype == MO_F32)
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_update_bulk_kernel<float>, 256, smem);
+        else
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, vote_update_bulk_kernel<bf16>, 256, smem);
+        if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+        const int64_t g = std::min<int64_t>(nchunks, static_cast<int64_t>(device_sm_count()) * per_sm);
+        if (w_dtype == MO_F32)
+            vote_update_bulk_kernel<float><<<static_cast<int>(g), 256, smem, s>>>(ptrs, M, nbits, thr,
+                                                                               static_cast<float*>(W), lr, nchunks);
+        else
+            vote_update_bulk_kernel<bf16><<<static_cast<int>(g), 256, smem, s>>>(ptrs, M, nbits, thr,
+                                                                              static_cast<bf16*>(W), lr, nchunks);
+        return cudaGetLastError();
+    }
     if (vec) {
+        const int per_sm = w_dtype == MO_F32 ? resident_blocks_per_sm(vote_update_vec_kernel<float>, 256)
+                                             : resident_blocks_per_sm(vote_update_vec_kernel<bf16>, 256);
+        const int64_t wave = static_cast<int64_t>(device_sm_count()) * per_sm;   // one resident wave
+        if (grid > wave) grid = static_cast<int>(wave);
         if (w_dtype == MO_F32)
             vote_update_vec_kernel<float><<<grid, 256, 0, s>>>(ptrs, M, nbits, thr, rows, cols, ld,
                                                                static_cast<float*>(W), lr, nwords);

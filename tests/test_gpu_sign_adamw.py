@@ -76,6 +76,25 @@ def test_vote_update_bit_exact(M, shape, ld, wdtype):
         assert torch.isnan(full[:, shape[1]:].float()).all()
 
 
+@pytest.mark.parametrize("M", [1, 2, 8, 16, 17])
+@pytest.mark.parametrize("shape", [(64, 128), (256, 512), (2048, 2048)])
+@pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
+def test_vote_update_chunked_path_bit_exact(M, shape, wdtype):
+    """Contiguous W with whole 8192-element chunks and up to 16 workers takes
+    the shared-memory streaming path (17 workers fall back); bit-exact both ways."""
+    rng = np.random.default_rng(7 * M + shape[1])
+    numel = shape[0] * shape[1]
+    bufs = [rng.integers(0, 2 ** 32, size=numel // 32, dtype=np.uint64).astype(np.uint32) for _ in range(M)]
+    words = [torch.from_numpy(b.view(np.int32).copy()).to(dev()) for b in bufs]
+    W = (0.02 * rng.standard_normal(shape)).astype(np.float32)
+    Wt = to_dev(W, wdtype)
+    W_stored = to_np(Wt)
+    mo.sign_vote_update(words, Wt, 1e-3)
+    torch.cuda.synchronize()
+    want = osg.vote_update(W_stored, bufs, 1e-3, "bf16" if wdtype == torch.bfloat16 else "f32")
+    assert np.array_equal(to_np(Wt), want)
+
+
 def test_vote_ties_go_plus():
     # M = 2 with opposite signs everywhere: every vote is a tie -> +1
     numel = 64 * 64
