@@ -325,6 +325,15 @@ __device__ __forceinline__ void load8(const bf16* p, float (&x)[8]) {
     }
 }
 
+__device__ __forceinline__ void unpack_bf16x8_pack(const uint4& u, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        x[2 * q] = __low2float(h[q]);
+        x[2 * q + 1] = __high2float(h[q]);
+    }
+}
+
 constexpr int kMaxPackBatch = 128;
 struct PackPtrs {
     const void* U[kMaxPackBatch];
@@ -369,12 +378,106 @@ __global__ void __launch_bounds__(256) sign_pack_vec_kernel(const __grid_constan
     }
 }
 
+// Bounded wait on an mbarrier phase (about 2 s of SM clock); false on timeout.
+__device__ __forceinline__ bool wait_phase_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+// Bulk path for contiguous bf16 matrices whose element count is a multiple of
+// kPackChunk: each block streams chunks of kPackChunk elements (of any
+// matrix of the batch) through a kPackStages-deep ring in shared memory, one
+// bulk copy per chunk; warps then read consecutive 16-byte pieces (8
+// elements -> one sign byte), and four lanes combine their bytes into a word.
+constexpr int kPackChunk = 8192;
+constexpr int kPackStages = 3;
+
+__global__ void __launch_bounds__(256) sign_pack_bulk_kernel(const __grid_constant__ PackPtrs pp,
+                                                             int64_t chunks_per_matrix, int64_t nchunks) {
+    extern __shared__ __align__(128) uint8_t psm[];
+    __shared__ __align__(8) uint64_t full[kPackStages];
+    constexpr uint32_t kBytes = kPackChunk * 2;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (t == 0) {
+        for (int s2 = 0; s2 < kPackStages; ++s2) mbar_init(smem_u32(&full[s2]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int64_t q, int st) {                 // thread 0
+        const int64_t m = q / chunks_per_matrix, c = q - m * chunks_per_matrix;
+        const uint32_t bar = smem_u32(&full[st]);
+        mbar_arrive_expect_tx(bar, kBytes);
+        bulk_load(smem_u32(psm + st * kBytes), static_cast<const bf16*>(pp.U[m]) + c * kPackChunk, kBytes, bar);
+    };
+    if (t == 0)
+        for (int s2 = 0; s2 < kPackStages; ++s2)
+            if (blockIdx.x + s2 * static_cast<int64_t>(gridDim.x) < nchunks) issue(blockIdx.x + s2 * gridDim.x, s2);
+    int k = 0;
+    bool ok = true;
+    for (int64_t q = blockIdx.x; q < nchunks; q += gridDim.x, ++k) {
+        const int st = k % kPackStages;
+        ok = wait_phase_bounded(smem_u32(&full[st]), (k / kPackStages) & 1);
+        if (!__syncthreads_and(ok)) break;                 // never expected: a bounded give-up
+        const int64_t m = q / chunks_per_matrix, c = q - m * chunks_per_matrix;
+        const uint4* src = reinterpret_cast<const uint4*>(psm + st * kBytes);
+        uint32_t* dst = pp.words[m] + c * (kPackChunk / 32);
+#pragma unroll
+        for (int it = 0; it < kPackChunk / 8 / 256; ++it) {
+            const int piece = it * 256 + warp * 32 + lane;           // 8 elements each
+            float x[8];
+            unpack_bf16x8_pack(src[piece], x);
+            uint32_t v = sign_byte(x) << (8 * (lane & 3));
+            v |= __shfl_xor_sync(0xffffffffu, v, 1);
+            v |= __shfl_xor_sync(0xffffffffu, v, 2);
+            if ((lane & 3) == 0) dst[piece >> 2] = v;
+        }
+        __syncthreads();                                   // the stage is read
+        if (t == 0) {
+            const int64_t qn = q + kPackStages * static_cast<int64_t>(gridDim.x);
+            if (qn < nchunks) issue(qn, st);
+        }
+    }
+    if (t == 0 && !ok) {
+        // let copies still landing in this block's shared memory finish
+        for (int s2 = 0; s2 < kPackStages; ++s2) (void)wait_phase_bounded(smem_u32(&full[s2]), (k / kPackStages) & 1);
+    }
+}
+
 cudaError_t launch_sign_pack_batched(const void* const* U, uint32_t* const* words, int M, int dtype, int64_t rows,
                                      int64_t cols, int64_t ld, cudaStream_t s) {
     const int64_t nwords = (rows * cols + 31) / 32;
     if (nwords == 0 || M <= 0) return cudaSuccess;
     bool vec = cols % 8 == 0 && ld % 8 == 0;
     for (int m = 0; m < M; ++m) vec = vec && (reinterpret_cast<uintptr_t>(U[m]) & 15u) == 0;
+    const bool bulk = vec && dtype == MO_BF16 && ld == cols && (rows * cols) % kPackChunk == 0;
+    if (bulk) {
+        PackPtrs pp{};
+        for (int m = 0; m < M; ++m) {
+            pp.U[m] = U[m];
+            pp.words[m] = words[m];
+        }
+        const int smem = kPackStages * kPackChunk * 2;
+        static std::atomic<uint64_t> attr_set{0};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        const uint64_t bit = uint64_t(1) << (dev & 63);
+        if (!(attr_set.load() & bit)) {
+            e = cudaFuncSetAttribute(sign_pack_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            attr_set.fetch_or(bit);
+        }
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sign_pack_bulk_kernel, 256, smem);
+        if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+        const int64_t cpm = rows * cols / kPackChunk, nchunks = cpm * M;
+        const int64_t g = std::min<int64_t>(nchunks, static_cast<int64_t>(device_sm_count()) * per_sm);
+        sign_pack_bulk_kernel<<<static_cast<int>(g), 256, smem, s>>>(pp, cpm, nchunks);
+        return cudaGetLastError();
+    }
     if (vec) {
         PackPtrs pp{};
         for (int m = 0; m < M; ++m) {
@@ -594,14 +697,6 @@ __global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_const
 constexpr int kVoteChunk = 8192;
 constexpr int kVoteChunkWords = kVoteChunk / 32;
 constexpr int kBulkVoters = 16;
-
-__device__ __forceinline__ bool wait_phase_bounded(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
 
 template <typename T>
 __global__ void __launch_bounds__(256) vote_update_bulk_kernel(const __grid_constant__ VotePtrs ptrs, int M,
