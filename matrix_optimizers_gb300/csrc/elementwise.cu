@@ -692,8 +692,8 @@ __global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_const
 // kVoteChunk elements through shared memory, two chunks in flight.  A chunk's
 // W and its kVoteChunk/32 words of every worker arrive by bulk copies on one
 // mbarrier; the 256 threads count one word each, then update the chunk in
-// shared memory with consecutive threads on consecutive elements; one bulk
-// store writes it back.  Same arithmetic as vote_update_vec_kernel.
+// registers and store it back with consecutive threads on consecutive
+// elements.  Same arithmetic as vote_update_vec_kernel.
 constexpr int kVoteChunk = 8192;
 constexpr int kVoteChunkWords = kVoteChunk / 32;
 constexpr int kBulkVoters = 16;
@@ -763,27 +763,21 @@ __global__ void __launch_bounds__(256) vote_update_bulk_kernel(const __grid_cons
         }
         vote[t] = gt | eq;
         __syncthreads();
-        T* w = reinterpret_cast<T*>(base);
+        const T* w = reinterpret_cast<const T*>(base);
+        T* wg = W + c * kVoteChunk;
 #pragma unroll 8
         for (int j = 0; j < 32; ++j) {
-            const int e = t + 256 * j;
+            const int e = t + 256 * j;                     // a warp stores 32 consecutive elements
             const float x = static_cast<float>(w[e]);
-            w[e] = static_cast<T>(((vote[e >> 5] >> (e & 31)) & 1u) ? (x - lr) : (x + lr));
+            wg[e] = static_cast<T>(((vote[e >> 5] >> (e & 31)) & 1u) ? (x - lr) : (x + lr));
         }
-        fence_proxy_async_smem();
-        __syncthreads();
+        __syncthreads();                                   // the stage is read
         if (t == 0) {
-            bulk_store(W + c * kVoteChunk, smem_u32(base), kWBytes);
-            bulk_commit();
             const int64_t cn = c + 2 * static_cast<int64_t>(gridDim.x);
-            if (cn < nchunks) {
-                bulk_wait_read_all();                      // the stage is free once the store has read it
-                issue(cn, st);
-            }
+            if (cn < nchunks) issue(cn, st);
         }
     }
     if (t == 0) {
-        bulk_wait_all();
         if (!ok) {
             // let copies still landing in this block's shared memory finish
             for (int s2 = 0; s2 < 2; ++s2) (void)wait_phase_bounded(smem_u32(&full[s2]), (k >> 1) & 1);
