@@ -19,9 +19,10 @@ extern "C" {
  * ns_orthogonalize / muon_step_batched use for these shapes (offsets are in
  * bytes from the workspace base).  Orientation: m = min(rows, cols),
  * n = max(rows, cols), transposed = rows > cols.
- *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong (ldx; X
- *              is kept in bf16 between steps, x_master = 0),
- *              gram = bf16 m x m (lda),
+ *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong in 8-column
+ *              blocks: element (i, j) at byte ((j/8)*ldx + i)*16 + (j%8)*2,
+ *              where ldx = m rounded up to 8 (X is kept in bf16 between
+ *              steps, x_master = 0); gram = bf16 m x m row-major (lda),
  *              poly = bf16 m x m (lda).
  *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong (x_master = 0),
  *              gram, poly = fp32 m x m.
@@ -52,10 +53,10 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
 int mo_debug_sm_count(void);
 
 /* Chooses between the two readings of the shared-memory descriptor strides
- * for the MN-major operand of the apply phase (64-element MN atoms 8 KB
- * apart, 8-row K groups 1 KB apart): (lbo, sbo) = (8192, 1024), the default,
- * or (1024, 8192).  Other values give MO_ERR_INVALID_ARG.  Process-wide;
- * affects launches issued after the call. */
+ * for the apply phase's MN-major operand (no swizzle: 8-row K groups 128 B
+ * apart, 8-column MN blocks 1 KB apart): (lbo, sbo) = (128, 1024), the
+ * default, or (1024, 128).  Other values give MO_ERR_INVALID_ARG.
+ * Process-wide; affects launches issued after the call. */
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
 /* Chooses the tile geometry of the bf16 tensor-core Newton-Schulz kernel:

@@ -80,9 +80,10 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS;
 }
 
-// Descriptor strides of the MN-major B operand (64-element MN atoms of 8 KB,
-// 8-row K groups of 1 KB).  Exposed to tests through the debug header.
-std::atomic<uint32_t> g_mn_lbo{8192};
+// Descriptor strides of the apply phase's MN-major B operand (no swizzle:
+// 8-row K groups 128 B apart, 8-column MN blocks 1 KB apart), as (lbo, sbo).
+// Exposed to tests through the debug header.
+std::atomic<uint32_t> g_mn_lbo{128};
 std::atomic<uint32_t> g_mn_sbo{1024};
 // How the tensor-core iterations are launched: 1 one fused cooperative launch
 // (when the grid fits on the device at once) ordered by per-matrix counters;
@@ -130,6 +131,7 @@ struct Job {
 
 struct Shape {
     int64_t m, n, ldx, lda;
+    int64_t xrows, xblocks;        // bf16 operand: rows of an 8-column block (m rounded to 8), blocks
     int transposed;
 };
 
@@ -140,8 +142,27 @@ Shape oriented(int64_t rows, int64_t cols) {
     s.n = s.transposed ? rows : cols;
     s.ldx = static_cast<int64_t>(align_up(static_cast<size_t>(s.n), 64));
     s.lda = static_cast<int64_t>(align_up(static_cast<size_t>(s.m), 64));
+    s.xrows = static_cast<int64_t>(align_up(static_cast<size_t>(s.m), 8));
+    s.xblocks = ceil_div(s.n, 8);
     return s;
 }
+
+// The bf16 operand X in 8-column blocks, viewed by TMA as 3D: 64 elements
+// (8 rows x 8 columns of one block, 128 contiguous bytes), row groups of 8,
+// column blocks.  A box of `rows` x `cols` of X lands in shared memory as
+// [column block][row][8 elements], the no-swizzle canonical layout.
+constexpr int kMapsPerMatrix = 8;    // 3 views of each operand buffer, Gram, polynomial
+bool encode_xop_map(CUtensorMap* map, const void* base, const Shape& s, int rows, int cols) {
+    cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(s.xrows / 8), static_cast<cuuint64_t>(s.xblocks)};
+    cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(s.xrows * 16)};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows / 8), static_cast<cuuint32_t>(cols / 8)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 
 struct MatBufs {
     size_t x_op[2], gram, poly;
@@ -206,7 +227,7 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
     L.mats = off;
     off = align_up(off + n * sizeof(MatDesc), 128);
     L.tmaps = off;
-    if (precision == MO_NS_BF16) off = align_up(off + n * 4 * sizeof(CUtensorMap), 128);
+    if (precision == MO_NS_BF16) off = align_up(off + n * kMapsPerMatrix * sizeof(CUtensorMap), 128);
     for (int ph = 0; ph < 3; ++ph) {
         L.tiles[ph] = off;
         off = align_up(off + static_cast<size_t>(L.ntiles[ph]) * sizeof(TileDesc), 128);
@@ -233,7 +254,8 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
     const size_t xe = precision == MO_NS_BF16 ? 2 : 4;
     for (size_t i = 0; i < n; ++i) {
         const Shape& s = L.shape[i];
-        const size_t xbytes = static_cast<size_t>(s.m) * s.ldx * xe;
+        const size_t xbytes = precision == MO_NS_BF16 ? static_cast<size_t>(s.xblocks) * s.xrows * 16
+                                                      : static_cast<size_t>(s.m) * s.ldx * xe;
         const size_t abytes = static_cast<size_t>(s.m) * s.lda * xe;
         MatBufs& b = L.buf[i];
         b.x_op[0] = off; off = align_up(off + xbytes, kBufAlign);
@@ -411,6 +433,7 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
         d.m = static_cast<int32_t>(s.m);
         d.n = static_cast<int32_t>(s.n);
         d.ldx = static_cast<int32_t>(s.ldx);
+        d.xrows = static_cast<int32_t>(s.xrows);
         d.lda = static_cast<int32_t>(s.lda);
         d.ld = j.ld;
         d.rows = static_cast<int32_t>(j.rows);
@@ -443,16 +466,25 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
         d.nt_apply = static_cast<int32_t>(apply_tiles(s.m, s.n, pair));
         d.deps = reinterpret_cast<int*>(base + L.deps) + 4 * i;
         if (o.precision == MO_NS_BF16) {
+            const int bn = pair ? kTcBN / 2 : kTcBN;     // B-operand columns one CTA loads
+            CUtensorMap* hm0 = htm + kMapsPerMatrix * i;
+            const CUtensorMap* dm0 = dtm + kMapsPerMatrix * i;
             for (int q = 0; q < 2; ++q) {
-                if (!encode_bf16_map(&htm[4 * i + q], d.x_op[q], s.m, s.n, s.ldx)) return MO_ERR_CUDA;
-                d.tm_x[q] = dtm + 4 * i + q;
+                if (!encode_xop_map(&hm0[3 * q + 0], d.x_op[q], s, kTcBM, kTcBK) ||
+                    !encode_xop_map(&hm0[3 * q + 1], d.x_op[q], s, bn, kTcBK) ||
+                    !encode_xop_map(&hm0[3 * q + 2], d.x_op[q], s, kTcBK, bn))
+                    return MO_ERR_CUDA;
+                d.tm_xa[q] = dm0 + 3 * q + 0;
+                d.tm_xb[q] = dm0 + 3 * q + 1;
+                d.tm_xn[q] = dm0 + 3 * q + 2;
             }
-            if (!encode_bf16_map(&htm[4 * i + 2], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            if (!encode_bf16_map(&htm[4 * i + 3], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            d.tm_gram = dtm + 4 * i + 2;
-            d.tm_poly = dtm + 4 * i + 3;
+            if (!encode_bf16_map(&hm0[6], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&hm0[7], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            d.tm_gram = dm0 + 6;
+            d.tm_poly = dm0 + 7;
         } else {
-            d.tm_x[0] = d.tm_x[1] = d.tm_gram = d.tm_poly = nullptr;
+            for (int q = 0; q < 2; ++q) d.tm_xa[q] = d.tm_xb[q] = d.tm_xn[q] = nullptr;
+            d.tm_gram = d.tm_poly = nullptr;
         }
     }
 
@@ -556,6 +588,28 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
 
     cudaError_t e = cudaMemcpyAsync(base, plan->stage.data(), L.ctl_bytes, cudaMemcpyHostToDevice, stream);
     if (e != cudaSuccess) return MO_ERR_CUDA;
+    if (tc) {
+        // The bf16 operand's padding is read by the tensor cores (inside whole
+        // 128-byte TMA lines) and must hold zeros: the rows from m up to a
+        // multiple of 8 in every block of both buffers, and the columns of the
+        // last block from n on (bf16(M) is written over the rest of that block).
+        for (size_t i = 0; i < jobs.size(); ++i) {
+            const Shape& sh = L.shape[i];
+            const MatBufs& b = L.buf[i];
+            if (sh.xrows > sh.m)
+                for (int q = 0; q < 2; ++q) {
+                    e = cudaMemset2DAsync(base + b.x_op[q] + sh.m * 16, static_cast<size_t>(sh.xrows) * 16, 0,
+                                          static_cast<size_t>(sh.xrows - sh.m) * 16, static_cast<size_t>(sh.xblocks),
+                                          stream);
+                    if (e != cudaSuccess) return MO_ERR_CUDA;
+                }
+            if (sh.n % 8 != 0) {
+                e = cudaMemsetAsync(base + b.x_op[0] + static_cast<size_t>(sh.xblocks - 1) * sh.xrows * 16, 0,
+                                    static_cast<size_t>(sh.xrows) * 16, stream);
+                if (e != cudaSuccess) return MO_ERR_CUDA;
+            }
+        }
+    }
 
     const MatDesc* dmats = reinterpret_cast<const MatDesc*>(base + L.mats);
     MomLaunch mp;
@@ -1060,7 +1114,7 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
     const MatBufs& b = L.buf[active];
     view->m = s.m;
     view->n = s.n;
-    view->ldx = s.ldx;
+    view->ldx = precision == MO_NS_BF16 ? s.xrows : s.ldx;   // bf16: rows of an 8-column block
     view->lda = s.lda;
     view->transposed = s.transposed;
     view->precision = precision;
@@ -1142,9 +1196,9 @@ int mo_debug_set_ns_fused(int on) {
 }
 
 int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo) {
-    // only the two readings of the MN-major 128-byte-swizzle layout; both keep
-    // every operand read inside the stage's 32 KB B buffer
-    const bool ok = (lbo == 8192u && sbo == 1024u) || (lbo == 1024u && sbo == 8192u);
+    // only the two readings of the no-swizzle MN-major layout; both keep every
+    // operand read inside the stage's B buffer
+    const bool ok = (lbo == 128u && sbo == 1024u) || (lbo == 1024u && sbo == 128u);
     if (!ok) return MO_ERR_INVALID_ARG;
     g_mn_lbo.store(lbo);
     g_mn_sbo.store(sbo);

@@ -104,6 +104,13 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
     return s;
 }
 
+// Element (i, j) of the NS operand: fp32 row-major (leading dimension ldx),
+// or bf16 in 8-column blocks of xrows rows.
+__device__ __forceinline__ int64_t xop_offset(const MatDesc& md, bool fp32, int i, int j) {
+    return fp32 ? static_cast<int64_t>(i) * md.ldx + j
+                : (static_cast<int64_t>(j >> 3) * md.xrows + i) * 8 + (j & 7);
+}
+
 // ------------------------------------------------------------ momentum_norm
 // Tile of 64 x 64 user elements per iteration, 256 threads: thread t owns
 // columns 4*(t%16)..+3 of rows t/16 + 16q, q = 0..3.
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) ss = fmaf(x[k], x[k], ss);
                 if (!md.transposed)
-                    store4(md.x_op[0], op_dt, static_cast<int64_t>(r) * md.ldx + c, nvalid, x);
+                    store4(md.x_op[0], op_dt, xop_offset(md, p.fp32_operand, r, c), nvalid, x);
             }
             if (md.transposed) {
 #pragma unroll
@@ -158,7 +165,6 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
             // c0 + xr, oriented columns = user rows r0 + seg .. +15
             void* dst = md.x_op[0];
             const int dt = op_dt;
-            const int64_t dld = md.ldx;
             const int xr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;
             const int orow = c0 + xr;
             if (orow < md.cols) {
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
                         float v[4];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) v[k] = tileT[xr][seg + 4 * g4 + k];
-                        store4(dst, dt, static_cast<int64_t>(orow) * dld + ocol, nv, v);
+                        store4(dst, dt, xop_offset(md, p.fp32_operand, orow, ocol), nv, v);
                     }
                 }
             }

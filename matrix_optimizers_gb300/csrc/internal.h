@@ -52,10 +52,15 @@ struct MatDesc {
     void* W;                   // update target or null
     void* out;                 // NS output target or null
     uint32_t* sign_words;      // fused sign + 1-bit pack target of the output, or null
-    void* x_op[2];             // NS operand ping-pong (bf16 or fp32), m x ldx
+    void* x_op[2];             // NS operand ping-pong: fp32 m x ldx row-major (fp32 mode), or bf16 in
+                               // 8-column blocks: element (i, j) at ((j / 8) * xrows + i) * 8 + j % 8
+    int32_t xrows;             // rows of one 8-column block of the bf16 operand (m rounded up to 8)
     void* gram;                // m x lda  (A = X X^T)
     void* poly;                // m x lda  (B = b A + c A^2)
-    const CUtensorMap* tm_x[2];
+    // bf16 operand views (3D: 64 elements = 8 rows x 8 columns of a block, row groups, column blocks)
+    const CUtensorMap* tm_xa[2];   // box 128 rows x 64 columns: A operand of the Gram phase
+    const CUtensorMap* tm_xb[2];   // box (256 or 128) rows x 64 columns: B operand of the Gram phase
+    const CUtensorMap* tm_xn[2];   // box 64 rows x (256 or 128) columns: B operand of the apply phase
     const CUtensorMap* tm_gram;
     const CUtensorMap* tm_poly;
     float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix),

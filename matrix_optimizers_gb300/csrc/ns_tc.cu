@@ -373,8 +373,13 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
 #pragma unroll
     for (int k = 0; k < 32; ++k) x[k] = scale * v[k];
     if (step + 1 < p.steps) {
+        // the next operand, in 8-column blocks: the warp's 32 rows of one block
+        // are 512 contiguous bytes (columns past n hold the accumulator's zeros)
         if (!row_ok) return;
-        store32(md.x_op[(step + 1) & 1], MO_BF16, static_cast<int64_t>(i) * md.ldx + j0, nv, x);
+        uint4* dst = static_cast<uint4*>(md.x_op[(step + 1) & 1]) + static_cast<int64_t>(j0 >> 3) * md.xrows + i;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (j0 + 8 * q < n) dst[static_cast<int64_t>(q) * md.xrows] = pack_bf16x8(&x[8 * q]);
         return;
     }
     if (md.sign_words != nullptr) {
@@ -457,6 +462,23 @@ __device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, 
     }
 }
 
+// TMA loads of one box, the pair form counting on the leader's barrier.
+template <bool kPair>
+__device__ __forceinline__ void load2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y) {
+    if constexpr (kPair)
+        tma_load_2d_pair(dst, m, bar, x, y);
+    else
+        tma_load_2d(dst, m, bar, x, y);
+}
+// blocked operand (3D view): box origin at row group y, column block z
+template <bool kPair>
+__device__ __forceinline__ void load3(uint32_t dst, const CUtensorMap* m, uint32_t bar, int y, int z) {
+    if constexpr (kPair)
+        tma_load_3d_pair(dst, m, bar, 0, y, z);
+    else
+        tma_load_3d(dst, m, bar, 0, y, z);
+}
+
 // Tiles of phase ph scheduled on schedule unit `unit` (a CTA, or a CTA pair).
 __device__ __forceinline__ int2 unit_tiles(const NsLaunch& p, int ph, int unit) {
     return unit < p.tc_ctas[ph] ? p.tc_ranges[ph][unit] : make_int2(0, 0);
@@ -468,6 +490,7 @@ __device__ __forceinline__ int2 unit_tiles(const NsLaunch& p, int ph, int unit) 
 template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constant__ NsLaunch p) {
     using G = Geo<kPair>;
+    constexpr int kBRows = G::kBBoxes * kBox;                 // B-operand rows (Gram) one CTA holds
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Ctl* ctl = reinterpret_cast<Ctl*>(smem + G::kStages * G::kStageBytes);
@@ -535,53 +558,53 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     const int j0 = td.tj * kTcBN + (kPair ? static_cast<int>(rank) * (kTcBN / 2) : 0);
                     const CUtensorMap* tma;
                     const CUtensorMap* tmb;
-                    if (ph == kGram) {
-                        tma = tmb = md.tm_x[step & 1];
-                    } else if (ph == kPoly) {
+                    if (ph == kGram) {                 // both from the blocked operand
+                        tma = md.tm_xa[step & 1];
+                        tmb = md.tm_xb[step & 1];
+                    } else if (ph == kPoly) {          // both from A (128-byte swizzle)
                         tma = tmb = md.tm_gram;
-                    } else {
+                    } else {                           // B (swizzled), then the blocked operand
                         tma = md.tm_poly;
-                        tmb = md.tm_x[step & 1];
+                        tmb = md.tm_xn[step & 1];
                     }
-                    for (int kb = 0; kb < td.nkb; ++kb) {
-                        const uint32_t empty = smem_u32(&ctl->empty[stage]);
-                        const uint32_t full = smem_u32(&ctl->full[stage]);
-                        if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) { ok = false; break; }
-                        if (leader) mbar_arrive_expect_tx(full, G::kTxBytes);
-                        ++armed[stage];
-                        const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
-                        const uint32_t sb = sa + kABytes;
-                        const int k0 = kb * kTcBK;
-                        // (the operand-major test stays outside the unrolled box loops: a
-                        // branch between the copies measured ~20% slower in every phase,
-                        // the producer thread's issue rate being on the critical path)
-                        if constexpr (kPair) {
-                            const uint32_t bar = mapa_shared(full, 0);   // the leader's barrier
-                            tma_load_2d_pair(sa, tma, bar, k0, i0);
-                            tma_load_2d_pair(sa + kBoxBytes, tma, bar, k0, i0 + kBox);
-                            if (!mn_b) {
-#pragma unroll
-                                for (int q = 0; q < G::kBBoxes; ++q)
-                                    tma_load_2d_pair(sb + q * kBoxBytes, tmb, bar, k0, j0 + q * kBox);
-                            } else {
-#pragma unroll
-                                for (int q = 0; q < G::kBBoxes; ++q)
-                                    tma_load_2d_pair(sb + q * kBoxBytes, tmb, bar, j0 + q * kBox, k0);
+                    // one K loop per phase, chosen once per tile: the copies differ by
+                    // phase, and any branch among them inside the loop measured ~20%
+                    // slower in every phase (the producer's issue rate is on the
+                    // critical path)
+                    auto k_loop = [&](auto&& load) {
+                        for (int kb = 0; kb < td.nkb; ++kb) {
+                            const uint32_t empty = smem_u32(&ctl->empty[stage]);
+                            const uint32_t full = smem_u32(&ctl->full[stage]);
+                            if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) {
+                                ok = false;
+                                return;
                             }
-                        } else {
-                            tma_load_2d(sa, tma, full, k0, i0);
-                            tma_load_2d(sa + kBoxBytes, tma, full, k0, i0 + kBox);
-                            if (!mn_b) {
-#pragma unroll
-                                for (int q = 0; q < G::kBBoxes; ++q)
-                                    tma_load_2d(sb + q * kBoxBytes, tmb, full, k0, j0 + q * kBox);
-                            } else {
-#pragma unroll
-                                for (int q = 0; q < G::kBBoxes; ++q)
-                                    tma_load_2d(sb + q * kBoxBytes, tmb, full, j0 + q * kBox, k0);
-                            }
+                            if (leader) mbar_arrive_expect_tx(full, G::kTxBytes);
+                            ++armed[stage];
+                            const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
+                            const uint32_t bar = kPair ? mapa_shared(full, 0) : full;   // the leader's barrier
+                            load(sa, sa + kABytes, bar, kb * kTcBK);
+                            if (++stage == G::kStages) { stage = 0; phase ^= 1u; }
                         }
-                        if (++stage == G::kStages) { stage = 0; phase ^= 1u; }
+                    };
+                    if (ph == kGram) {
+                        k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
+                            load3<kPair>(sa, tma, bar, i0 >> 3, k0 >> 3);
+                            load3<kPair>(sb, tmb, bar, j0 >> 3, k0 >> 3);
+                        });
+                    } else if (ph == kPoly) {
+                        k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
+                            load2<kPair>(sa, tma, bar, k0, i0);
+                            load2<kPair>(sa + kBoxBytes, tma, bar, k0, i0 + kBox);
+#pragma unroll
+                            for (int q = 0; q < G::kBBoxes; ++q) load2<kPair>(sb + q * kBoxBytes, tmb, bar, k0, j0 + q * kBox);
+                        });
+                    } else {
+                        k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
+                            load2<kPair>(sa, tma, bar, k0, i0);
+                            load2<kPair>(sa + kBoxBytes, tma, bar, k0, i0 + kBox);
+                            load3<kPair>(sb, tmb, bar, k0 >> 3, j0 >> 3);
+                        });
                     }
                 }
             }
@@ -618,6 +641,28 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 const int2 range = unit_tiles(p, ph, unit);
                 const bool mn_b = ph == kApply;
                 const uint32_t idesc = mn_b ? p.idesc_apply : p.idesc_sym;
+                // Descriptors with a zero address field, and the per-16-wide-K-step
+                // address increments (16-byte units), by phase: Gram reads both
+                // operands blocked (no swizzle, K-major: 8-column blocks rows x 16 B
+                // apart, 8-row groups 128 B apart); poly reads A swizzled twice;
+                // apply reads B swizzled and the blocked operand MN-major (8-row K
+                // groups 128 B apart, 8-column blocks 1 KB apart; 16 K rows = 256 B)
+                uint64_t adesc0, bdesc0;
+                uint32_t a_step, b_step;
+                if (ph == kGram) {
+                    adesc0 = sdesc_noswz(0, kTcBM * 16, 128);
+                    bdesc0 = sdesc_noswz(0, kBRows * 16, 128);
+                    a_step = (2 * kTcBM * 16) >> 4;
+                    b_step = (2 * kBRows * 16) >> 4;
+                } else if (ph == kPoly) {
+                    adesc0 = bdesc0 = sdesc_sw128(0, 16, 1024);
+                    a_step = b_step = 32 >> 4;
+                } else {
+                    adesc0 = sdesc_sw128(0, 16, 1024);
+                    bdesc0 = sdesc_noswz(0, p.mn_lbo, p.mn_sbo);
+                    a_step = 32 >> 4;
+                    b_step = 256 >> 4;
+                }
                 for (int t = 0; t < range.y && ok; ++t, ++q) {
                     const TileDesc td = p.tc_tiles[ph][range.x + t];
                     const int acc = q & 1;
@@ -638,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         const uint32_t sb = sa + kABytes;
 #pragma unroll
                         for (int k = 0; k < kTcBK / 16; ++k) {
-                            const uint64_t ad = sdesc_sw128(sa + k * 32, 16, 1024);
-                            const uint64_t bd = mn_b ? sdesc_sw128(sb + k * 16 * 128, p.mn_lbo, p.mn_sbo)
-                                                     : sdesc_sw128(sb + k * 32, 16, 1024);
+                            // shared addresses stay below 256 KB: the 14-bit field never carries
+                            const uint64_t ad = adesc0 + ((sa >> 4) + k * a_step);
+                            const uint64_t bd = bdesc0 + ((sb >> 4) + k * b_step);
                             if constexpr (kPair)
                                 umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                             else

@@ -157,8 +157,8 @@ def test_debug_view_offsets_are_disjoint():
         v = B.mo_debug_ns_view(shapes, i)
         assert (v.m, v.n) == ((100, 300) if i < 2 else (64, 64))
         assert v.transposed == (1 if i == 1 else 0)
-        assert v.ldx % 64 == 0 and v.lda % 64 == 0
-        xb = v.m * v.ldx * 2
+        assert v.ldx % 8 == 0 and v.ldx >= v.m and v.lda % 64 == 0     # bf16 operand: 8-column blocks
+        xb = -(-v.n // 8) * v.ldx * 16
         assert v.x_master == 0                                # X stays in bf16 between steps
         spans += [(v.x_op[0], xb), (v.x_op[1], xb),
                   (v.gram, v.m * v.lda * 2), (v.poly, v.m * v.lda * 2)]

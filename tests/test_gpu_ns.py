@@ -44,7 +44,10 @@ def test_phases_individually(shape):
     Xo = X.T if v.transposed else X
     s = np.linalg.norm(Xo.astype(np.float32).astype(np.float64))
     Xb = ob.round_bf16(Xo.astype(np.float32).astype(np.float64))        # operand the kernels read
-    xb_dev = to_np(ws_view(ws, v.x_op[0], (m, n), torch.bfloat16, v.ldx))
+    # the bf16 operand lives in 8-column blocks of v.ldx rows: [block][row][8]
+    nb = -(-n // 8)
+    blk = ws[v.x_op[0]: v.x_op[0] + nb * v.ldx * 16].view(torch.bfloat16).view(nb, v.ldx, 8)
+    xb_dev = to_np(blk[:, :m, :].permute(1, 0, 2).reshape(m, nb * 8)[:, :n])
     assert np.array_equal(xb_dev, Xb)
     gram = to_np(ws_view(ws, v.gram, (m, m), torch.bfloat16, v.lda))
     want_gram = Xb @ Xb.T / s ** 2
@@ -132,9 +135,9 @@ def test_mn_descriptor_reading():
     want = om.newton_schulz(X.astype(np.float32).astype(np.float64))
     good = rel_fro(_ns([X])[0][0], want)
     try:
-        B.mo_debug_set_mn_strides(1024, 8192)
+        B.mo_debug_set_mn_strides(1024, 128)
         other = rel_fro(_ns([X])[0][0], want)
     finally:
-        B.mo_debug_set_mn_strides(8192, 1024)
+        B.mo_debug_set_mn_strides(128, 1024)
     assert good < NS_BF16_TOL
     assert not other < NS_BF16_TOL
