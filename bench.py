@@ -385,9 +385,10 @@ def run_gb300(args, rank, world, local_rank, dist):
         # and group k-2's weights are copied out on a third, so the host
         # traffic overlaps the kernels.  Each group is one library call (its own
         # workspace); the Sign-Muon workers' packed signs all feed one vote.
-        # default: about one group per 200 MB of host traffic, 1 to 8 groups
-        n_auto = int(round((sum(g.numel() for g in hG) + sum(w.numel() for w in hW)) * 4 / 200e6))
-        n_groups = max(1, min(args.e2e_groups if args.e2e_groups > 0 else max(1, min(8, n_auto)), len(shapes)))
+        # default: about one group per 170 MB of host traffic, 2 to 8 groups
+        # (measured best: 8 for the 7B share and ragged500, 4 for gpt_small, 2 for Sign-Muon)
+        n_auto = int(round((sum(g.numel() for g in hG) + sum(w.numel() for w in hW)) * 4 / 170e6))
+        n_groups = max(1, min(args.e2e_groups if args.e2e_groups > 0 else max(2, min(8, n_auto)), len(shapes)))
         sizes = [r * c for r, c in shapes]
         groups, cur, acc = [], [], 0
         for i, sz in enumerate(sizes):
@@ -652,7 +653,7 @@ def main():
                     help="NS tile geometry: 128x256 per CTA or 256x256 per CTA pair (default: the library's)")
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="matrix groups of the end-to-end step (copies of one overlap the kernels of another); "
-                         "0: one per ~200 MB of host traffic, at most 8")
+                         "0: one per ~170 MB of host traffic, 2 to 8")
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
