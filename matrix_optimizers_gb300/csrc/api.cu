@@ -570,6 +570,12 @@ int get_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair, i
 
 // Uploads the (cached) control block for `jobs` into `ws` and launches the
 // whole path on `stream`.
+// Launch errors that mean the launch was refused before anything ran.
+bool launch_refused(cudaError_t e) {
+    return e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorLaunchOutOfResources ||
+           e == cudaErrorInvalidConfiguration || e == cudaErrorNotSupported || e == cudaErrorInvalidClusterSize;
+}
+
 int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_bytes, cudaStream_t stream) {
     if (jobs.empty()) return MO_OK;
     int st = validate_ws(ws, ws_bytes, 0);
@@ -684,7 +690,14 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     const bool fuse = tc && mode != 0 && levels - lv_fuse > 1 && units_fused * cta_per_unit <= tc_capacity(pair);
     for (int lv = 0; lv < levels;) {
         const int lv1 = fuse && lv >= lv_fuse ? levels : lv + 1;
-        if ((e = launch_levels(lv, lv1)) != cudaSuccess) return MO_ERR_CUDA;
+        e = launch_levels(lv, lv1);
+        if (e != cudaSuccess && lv1 - lv > 1 && launch_refused(e)) {
+            // the runtime refused the cooperative launch (another client holding
+            // SMs, a profiler, ...): nothing ran, so run the levels one by one
+            (void)cudaGetLastError();
+            for (int l = lv; l < lv1 && (e = launch_levels(l, l + 1)) == cudaSuccess; ++l) {}
+        }
+        if (e != cudaSuccess) return MO_ERR_CUDA;
         if (lv == 0 && o.spectral_iters > 0) {
             // spectral scale: power iteration on the first Gram matrix, folded
             // into the first polynomial and apply through the per-matrix scales
