@@ -16,7 +16,8 @@ HBM; `e2e` is the same step through the same call with the gradients copied
 host->device and the weights device->host inside the timed region; `roofline`
 covers the dominant kernel (the tensor-core NS GEMM) from CUDA events recorded
 around each launch during the timed steps; `legs` times the Sign-Muon pack
-and vote kernels and the 50M-value AdamW tail against HBM.
+and vote kernels (8 workers at 2048^2, and at 8192^2 where the fixed cost of
+a launch is amortised) and the 50M-value AdamW tail against HBM.
 ``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
 workload instead (the reference arm).
 """
@@ -40,8 +41,8 @@ METRIC = "Muon step matrices/s and NS TFLOP/s (fraction of bf16 peak); vote GB/s
 # shape the kernel and its schedule hash to the value recorded with it.
 PROFILED_TRAFFIC = {
     ("llama7b_owner0", "fused"): {
-        "bytes_per_launch": 36.24e9 + 19.08e9,
-        "sources_sha256": "f2b088ef8818642c0ff21c7cd0cf0465ff32f421323c20a8327b2fedcce3cb26",
+        "bytes_per_launch": 36.43e9 + 19.09e9,
+        "sources_sha256": "487e475a6b8cacb6105f722a42d99fd404e44ba2352c22b5fb0a973827526845",
         "profile": "profiles/launches_llama7b_owner0.md",
     },
 }
@@ -536,6 +537,25 @@ def run_legs(dev, peaks, reps=20):
                              "ms": tc, "gbs": copy_bytes / (tc * 1e-3) / 1e9,
                              "frac": copy_bytes / (tc * 1e-3) / 1e9 / hbm, "bytes": copy_bytes}
     del U_sets, words_sets, W_sets, W_dst
+    # The same two kernels at 8192^2 per worker (16x the elements), where the
+    # fixed cost of a launch is amortised: each launch alone moves more than
+    # L2 holds (pack 1.07 GB; vote 0.6 GB, over two W buffers in turn).
+    nl = 8192
+    U_big = [torch.randn(nl, nl, device=dev, generator=g).bfloat16() for _ in range(8)]
+    words_big = [torch.empty(nl * nl // 32, dtype=torch.int32, device=dev) for _ in range(8)]
+    W_big = [torch.randn(nl, nl, device=dev, generator=g) for _ in range(2)]
+    pkl = graph_ms_per_launch([lambda: mo.sign_pack_batched(U_big, words_big)] * 2)
+    vtl = graph_ms_per_launch([(lambda k=k: mo.sign_vote_update(words_big, W_big[k], 1e-3)) for k in range(2)])
+    tpl, tvl = float(np.median(pkl)), float(np.median(vtl))
+    pack_bytes_l = 8 * nl * nl * (2 + 1 / 8)
+    vote_bytes_l = 8 * nl * nl / 8 + nl * nl * 8
+    out["pack_8192"] = {"workers": 8, "numel_per_worker": nl * nl, "ms_for_8": tpl,
+                        "gbs": pack_bytes_l / (tpl * 1e-3) / 1e9, "frac": pack_bytes_l / (tpl * 1e-3) / 1e9 / hbm,
+                        "bytes": pack_bytes_l, "l2": "each launch moves 1.07 GB"}
+    out["vote_8192"] = {"workers": 8, "numel": nl * nl, "ms": tvl, "gbs": vote_bytes_l / (tvl * 1e-3) / 1e9,
+                        "frac": vote_bytes_l / (tvl * 1e-3) / 1e9 / hbm, "bytes": vote_bytes_l,
+                        "l2": "each launch moves 0.60 GB; two W buffers in turn"}
+    del U_big, words_big, W_big
     numel = 50_000_000
     t = tail_inputs(numel)
     tt = {k: torch.from_numpy(t[k]).to(dev) for k in ("W", "g", "m", "v")}

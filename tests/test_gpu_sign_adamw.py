@@ -95,6 +95,23 @@ def test_vote_update_chunked_path_bit_exact(M, shape, wdtype):
     assert np.array_equal(to_np(Wt), want)
 
 
+@pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
+def test_vote_update_chunked_path_ring_wraps(wdtype):
+    """4096^2 with 8 workers: 2048 chunks over one resident wave of blocks, so
+    every block reuses both stages of its ring several times; bit-exact."""
+    rng = np.random.default_rng(41)
+    shape = (4096, 4096)
+    numel = shape[0] * shape[1]
+    bufs = [rng.integers(0, 2 ** 32, size=numel // 32, dtype=np.uint64).astype(np.uint32) for _ in range(8)]
+    words = [torch.from_numpy(b.view(np.int32).copy()).to(dev()) for b in bufs]
+    Wt = to_dev((0.02 * rng.standard_normal(shape)).astype(np.float32), wdtype)
+    W_stored = to_np(Wt)
+    mo.sign_vote_update(words, Wt, 1e-3)
+    torch.cuda.synchronize()
+    want = osg.vote_update(W_stored, bufs, 1e-3, "bf16" if wdtype == torch.bfloat16 else "f32")
+    assert np.array_equal(to_np(Wt), want)
+
+
 def test_vote_ties_go_plus():
     # M = 2 with opposite signs everywhere: every vote is a tie -> +1
     numel = 64 * 64
