@@ -399,6 +399,32 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     }
 }
 
+// Last NS step with the weight update: while the epilogue waits for the
+// current tile, pull this lane's W lines of the CTA's next apply tile into L2,
+// so that the update's loads find them there instead of waiting on DRAM.
+// The lane's row (row_off within the tile) and the slice column col0 follow
+// the epilogue's own mapping; each 32-column chunk the update reads is one
+// line per lane (W row i, or in the transposed frame W row j0 + lane).
+__device__ __noinline__ void prefetch_update_tile(const NsLaunch& p, int tile, int tile_rows, int row_off,
+                                                  int col0, int lane) {
+    const TileDesc td = p.tc_tiles[kApply][tile];
+    const MatDesc& md = p.mats[td.mat];
+    const int i = td.ti * tile_rows + row_off;
+    if (md.W == nullptr || md.sign_words != nullptr) return;
+    const char* w = static_cast<const char*>(md.W);
+    const int esz = md.w_dtype == MO_F32 ? 4 : 2;
+#pragma unroll
+    for (int ch = 0; ch < kEpiSliceCols / 32; ++ch) {
+        const int j0 = td.tj * kTcBN + col0 + ch * 32;
+        if (!md.transposed) {
+            if (i < md.m && j0 < md.n) prefetch_l2(w + (static_cast<int64_t>(i) * md.ld + j0) * esz);
+        } else {
+            const int r0 = i - lane;
+            if (r0 < md.m && j0 + lane < md.n) prefetch_l2(w + (static_cast<int64_t>(j0 + lane) * md.ld + r0) * esz);
+        }
+    }
+}
+
 // ------------------------------------------------- fused-launch dependencies
 // A fused launch runs several (step, phase) levels; a tile of level (t, ph)
 // of matrix md may start once, within this launch, every tile it reads or
@@ -725,11 +751,16 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
         for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
             const int ph = lv % 3, step = lv / 3;
             const int2 range = unit_tiles(p, ph, unit);
+            const bool prefetch_w = ph == kApply && step + 1 == p.steps && p.apply_update;
             for (int t = 0; t < range.y; ++t, ++q) {
                 const TileDesc td = p.tc_tiles[ph][range.x + t];
                 const MatDesc& md = p.mats[td.mat];
                 const int acc = q & 1;
                 const uint32_t acc_phase = (q >> 1) & 1;
+                if (prefetch_w && t + 1 < range.y)
+                    prefetch_update_tile(p, range.x + t + 1, G::kTileRows,
+                                         static_cast<int>(rank) * kTcBM + quarter * 32 + lane, slice * kEpiSliceCols,
+                                         lane);
                 ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }          // warp-uniform exit
                 tc_fence_after();
