@@ -402,15 +402,19 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
 // Last NS step with the weight update: while the epilogue waits for the
 // current tile, pull this lane's W lines of the CTA's next apply tile into L2,
 // so that the update's loads find them there instead of waiting on DRAM.
+// Only for short K (= m): a long tile hides the update's latency anyway, and
+// over its longer period the operand stream evicts part of the prefetched
+// lines, which are then read twice.
 // The lane's row (row_off within the tile) and the slice column col0 follow
 // the epilogue's own mapping; each 32-column chunk the update reads is one
 // line per lane (W row i, or in the transposed frame W row j0 + lane).
+constexpr int kPrefetchUpdateMaxK = 2048;
 __device__ __noinline__ void prefetch_update_tile(const NsLaunch& p, int tile, int tile_rows, int row_off,
                                                   int col0, int lane) {
     const TileDesc td = p.tc_tiles[kApply][tile];
     const MatDesc& md = p.mats[td.mat];
     const int i = td.ti * tile_rows + row_off;
-    if (md.W == nullptr || md.sign_words != nullptr) return;
+    if (md.W == nullptr || md.sign_words != nullptr || md.m > kPrefetchUpdateMaxK) return;
     const char* w = static_cast<const char*>(md.W);
     const int esz = md.w_dtype == MO_F32 ? 4 : 2;
 #pragma unroll
