@@ -793,15 +793,20 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     else if (row_ok)
                         epi_symmetric(p, md, ph, step, i, j0, v);
                 }
+                // the accumulator is in registers by now: hand it back to the
+                // MMA warp before waiting for this tile's stores to drain
                 tc_fence_before();
-                if (p.deps) fence_proxy_async_global();   // the stores above feed later TMA loads
                 __syncwarp();
                 if (lane == 0) {
                     if (leader)
                         mbar_arrive(smem_u32(&ctl->tempty[acc]));
                     else
                         mbar_arrive_cluster(tempty_leader[acc]);
-                    if (p.deps) red_release_gpu_add(deps_of(p, md).cnt + ph, 1);
+                }
+                if (p.deps) {
+                    fence_proxy_async_global();   // the stores above feed later TMA loads
+                    __syncwarp();
+                    if (lane == 0) red_release_gpu_add(deps_of(p, md).cnt + ph, 1);
                 }
             }
         }
