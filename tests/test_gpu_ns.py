@@ -72,6 +72,39 @@ def test_ns_bf16_vs_oracle(shape):
     assert rel_fro(got, want) < NS_BF16_TOL
 
 
+@pytest.mark.parametrize("shape", [(64, 8192), (8192, 64), (72, 4104)])
+def test_ns_bf16_extreme_aspect(shape):
+    """One row tile against a K of thousands in the Gram phase, and dozens of
+    apply tiles per row tile (aspect ratios up to 1:128)."""
+    X = np.random.default_rng(sum(shape) + 2).standard_normal(shape)
+    got = _ns([X])[0][0]
+    want = om.newton_schulz(X.astype(np.float32).astype(np.float64))
+    assert rel_fro(got, want) < NS_BF16_TOL
+
+
+@pytest.mark.parametrize("precision", [mo.MO_NS_BF16, mo.MO_NS_FP32])
+def test_ns_rank_deficient(precision):
+    """Rank-5 input.  Zero is a fixed point of the quintic, but an unstable one
+    (slope a = 3.4445), so rounding noise in the null space grows step by step.
+    In fp32 the output matches the oracle in full.  In bf16 that noise reaches
+    singular values near 0.16 (the rounding model puts it at 0.158), so the
+    check is on the part of the output in the input's row and column spaces,
+    which carries the result, with the null-space part bounded."""
+    rng = np.random.default_rng(8)
+    X = rng.standard_normal((192, 5)) @ rng.standard_normal((5, 320))
+    x32 = X.astype(np.float32).astype(np.float64)
+    got = _ns([X], precision=precision)[0][0]
+    want = om.newton_schulz(x32)
+    if precision == mo.MO_NS_FP32:
+        assert rel_fro(got, want) < NS_FP32_TOL
+        return
+    U, _, Vt = np.linalg.svd(x32, full_matrices=False)
+    Q, P = U[:, :5] @ U[:, :5].T, Vt[:5].T @ Vt[:5]
+    assert rel_fro(Q @ got @ P, want) < NS_BF16_TOL
+    sv = np.linalg.svd(got, compute_uv=False)
+    assert sv[5] < 0.4 * sv[0]
+
+
 def test_ns_bf16_batch_mixed_shapes_and_ld():
     rng = np.random.default_rng(7)
     shapes = [(256, 512), (512, 256), (96, 160), (384, 384), (72, 576)]
