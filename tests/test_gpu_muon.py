@@ -9,6 +9,7 @@ from oracle import adamw as oa
 from oracle import muon as om
 from oracle import planner as oplan
 from oracle import sign as osg
+from tests.ns_rounding_model import model_rel_err
 from tests.gpu_helpers import (MOM_TOL, NS_BF16_SPECTRAL_TOL, NS_BF16_TOL, NS_FP32_TOL, dev, rel_fro, to_dev,
                                to_np, workspace)
 from workloads import (CONFIGS, llama7b_shapes, matrix_inputs, matrix_set_inputs, ragged_shapes,
@@ -76,6 +77,24 @@ def test_gpt_small_full_step_with_tail():
         worst = max(worst, _check_update(Ws[i], inp, c["mu"], c["lr"], NS_BF16_TOL))
     Wt, _, _ = oa.adamw_step(t["W"], t["g"], t["m"], t["v"], 1, lr=c["tail_lr"])
     assert np.max(np.abs(tW.cpu().numpy() - Wt)) < 1e-8
+
+
+def test_many_tiny_matrices_one_step():
+    """300 matrices of 8 to 256 rows and columns, each one or a few tiles, so
+    that every CTA holds tiles of many matrices.  This exercises the grouped
+    launch, its per-matrix counters and the transposed frame."""
+    rng = np.random.default_rng(12)
+    shapes = [(8 * int(rng.integers(1, 9)), 8 * int(rng.integers(1, 33))) for _ in range(300)]
+    inputs = matrix_set_inputs(shapes)
+    cfg = mo.make_cfg(mu=0.95, lr=0.02)
+    Ws, _ = _run(inputs, cfg)
+    for w, inp in zip(Ws, inputs):
+        # M1 = G here (M0 = 0).  For m of 32 to 48 with a tight spectrum, bf16
+        # NS itself lands just above 2e-2 (the rounding model reaches 2.26e-2
+        # on 32 x 240), so each matrix's bound is the larger of 2e-2 and 1.5x
+        # the model's error for it
+        tol = max(NS_BF16_TOL, 1.5 * model_rel_err(inp["G"].astype(np.float32).astype(np.float64)))
+        _check_update(w, inp, 0.95, 0.02, tol)
 
 
 def test_weight_decay_and_update_scale():

@@ -22,34 +22,10 @@ Both are less accurate than the folded, consistent bf16 operator.
 """
 import numpy as np
 import pytest
-import torch
 
 from oracle import muon as om
 from tests.gpu_helpers import NS_BF16_SPECTRAL_TOL, NS_BF16_TOL
-
-A, B, C = om.NS_A, om.NS_B, om.NS_C
-
-
-def _bf(x):
-    return torch.from_numpy(np.asarray(x, np.float32)).bfloat16().double().numpy()
-
-
-def _f32(x):
-    return np.asarray(x, np.float32).astype(np.float64)
-
-
-def _ns_bf16_model(X0, steps=5, form="folded"):
-    Xf = _f32(X0)
-    Xb = _bf(Xf)
-    for _ in range(steps):
-        Ab = _bf(_f32(Xb @ Xb.T))
-        P = _f32(B * Ab + C * _f32(Ab @ Ab))
-        if form == "folded":
-            Xf = _f32(_bf(P + A * np.eye(len(P))) @ Xb)
-        else:
-            Xf = _f32(A * (Xf if form == "fp32_master" else Xb) + _bf(P) @ Xb)
-        Xb = _bf(Xf)
-    return Xf
+from tests.ns_rounding_model import ns_bf16_model
 
 
 @pytest.mark.parametrize("shape", [(96, 200), (256, 512)])
@@ -63,7 +39,7 @@ def test_bf16_model_error_levels(shape):
         for key, X0 in (("f", F), ("s", F / s)):
             ref = om.ns_iterate(X0)
             for form in forms:
-                err = np.linalg.norm(_ns_bf16_model(X0, form=form) - ref) / np.linalg.norm(ref)
+                err = np.linalg.norm(ns_bf16_model(X0, form=form) - ref) / np.linalg.norm(ref)
                 worst[key, form] = max(worst.get((key, form), 0.0), err)
     assert worst["f", "folded"] < 0.65 * NS_BF16_TOL
     assert worst["s", "folded"] < 0.8 * NS_BF16_SPECTRAL_TOL
