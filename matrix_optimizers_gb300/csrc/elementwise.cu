@@ -697,10 +697,13 @@ __global__ void __launch_bounds__(256) vote_update_vec_kernel(const __grid_const
 // kVoteChunk, with up to kBulkVoters workers: each block streams chunks of
 // kVoteChunk elements through shared memory, two chunks in flight.  A chunk's
 // W and its kVoteChunk/32 words of every worker arrive by bulk copies on one
-// mbarrier; the 256 threads count one word each, then update the chunk in
-// registers and store it back with consecutive threads on consecutive
-// elements.  Same arithmetic as vote_update_vec_kernel.
-constexpr int kVoteChunk = 8192;
+// mbarrier; the first kVoteChunkWords threads count one word each, then all
+// 256 update the chunk in registers and store it back with consecutive
+// threads on consecutive elements.  Same arithmetic as vote_update_vec_kernel.
+// 4096-element chunks keep the per-SM share even on small matrices: a 2048^2 W
+// is 1024 chunks over one resident wave of 5 blocks per SM (6 or 7 chunks per
+// SM), where 8192-element chunks left 3 or 4 per SM.
+constexpr int kVoteChunk = 4096;
 constexpr int kVoteChunkWords = kVoteChunk / 32;
 constexpr int kBulkVoters = 16;
 
@@ -743,36 +746,38 @@ __global__ void __launch_bounds__(256) vote_update_bulk_kernel(const __grid_cons
         uint8_t* base = vsm + st * stage_bytes;
         const uint32_t* wd = reinterpret_cast<const uint32_t*>(base + kWBytes);
         // bit-sliced count of +1 votes of word t over the M workers
-        uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int m = 0; m < M; ++m) {
-            uint32_t x = wd[m * kVoteChunkWords + t];
+        if (t < kVoteChunkWords) {
+            uint32_t cnt[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            for (int m = 0; m < M; ++m) {
+                uint32_t x = wd[m * kVoteChunkWords + t];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < 8; ++j) {
+                    if (j < nbits) {
+                        const uint32_t carry = cnt[j] & x;
+                        cnt[j] ^= x;
+                        x = carry;
+                    }
+                }
+            }
+            uint32_t gt = 0u, eq = 0xffffffffu;
+#pragma unroll
+            for (int j = 7; j >= 0; --j) {
                 if (j < nbits) {
-                    const uint32_t carry = cnt[j] & x;
-                    cnt[j] ^= x;
-                    x = carry;
+                    if ((thr >> j) & 1u) {
+                        eq &= cnt[j];
+                    } else {
+                        gt |= eq & cnt[j];
+                        eq &= ~cnt[j];
+                    }
                 }
             }
+            vote[t] = gt | eq;
         }
-        uint32_t gt = 0u, eq = 0xffffffffu;
-#pragma unroll
-        for (int j = 7; j >= 0; --j) {
-            if (j < nbits) {
-                if ((thr >> j) & 1u) {
-                    eq &= cnt[j];
-                } else {
-                    gt |= eq & cnt[j];
-                    eq &= ~cnt[j];
-                }
-            }
-        }
-        vote[t] = gt | eq;
         __syncthreads();
         const T* w = reinterpret_cast<const T*>(base);
         T* wg = W + c * kVoteChunk;
 #pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < kVoteChunk / 256; ++j) {
             const int e = t + 256 * j;                     // a warp stores 32 consecutive elements
             const float x = static_cast<float>(w[e]);
             wg[e] = static_cast<T>(((vote[e >> 5] >> (e & 31)) & 1u) ? (x - lr) : (x + lr));

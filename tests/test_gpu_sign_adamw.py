@@ -97,8 +97,9 @@ def test_vote_update_chunked_path_bit_exact(M, shape, wdtype):
 
 @pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
 def test_vote_update_chunked_path_ring_wraps(wdtype):
-    """4096^2 with 8 workers: 2048 chunks over one resident wave of blocks, so
-    every block reuses both stages of its ring several times; bit-exact."""
+    """4096^2 with 8 workers: 4096 chunks of 4096 elements over one resident
+    wave of blocks, so every block reuses both stages of its ring several
+    times; bit-exact."""
     rng = np.random.default_rng(41)
     shape = (4096, 4096)
     numel = shape[0] * shape[1]
