@@ -77,11 +77,12 @@ def test_vote_update_bit_exact(M, shape, ld, wdtype):
 
 
 @pytest.mark.parametrize("M", [1, 2, 8, 16, 17])
-@pytest.mark.parametrize("shape", [(64, 128), (256, 512), (2048, 2048)])
+@pytest.mark.parametrize("shape", [(64, 64), (64, 192), (64, 128), (256, 512), (2048, 2048)])
 @pytest.mark.parametrize("wdtype", [torch.float32, torch.bfloat16])
 def test_vote_update_chunked_path_bit_exact(M, shape, wdtype):
-    """Contiguous W with whole 8192-element chunks and up to 16 workers takes
-    the shared-memory streaming path (17 workers fall back); bit-exact both ways."""
+    """Contiguous W with whole 4096-element chunks (one, an odd three, ...) and
+    up to 16 workers takes the shared-memory streaming path (17 workers fall
+    back); bit-exact both ways."""
     rng = np.random.default_rng(7 * M + shape[1])
     numel = shape[0] * shape[1]
     bufs = [rng.integers(0, 2 ** 32, size=numel // 32, dtype=np.uint64).astype(np.uint32) for _ in range(M)]
