@@ -6,8 +6,9 @@ all device memory), or a latency-critical loop where a cudaMalloc would
 synchronise the device.  For them the library runs Newton-Schulz on a fixed
 scratch array compiled into it.  These tests call that entry point through the
 C ABI and check it against ns_orthogonalize with a caller workspace, on two
-calls in a row, so the second call runs over the first call's leftovers in
-the shared scratch.  This file is collected last on purpose.
+calls in a row of the same shape and then of another shape, so each later
+call runs over an earlier call's leftovers in the shared scratch.  This file
+is collected last on purpose.
 """
 import numpy as np
 import pytest
@@ -35,13 +36,18 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         X = np.random.default_rng(seed).standard_normal(shape).astype(np.float32)
         Xt = torch.from_numpy(X).to(dev()).to(in_dt)
         ref = _with_workspace(Xt, out_dt)
-        out = torch.full(shape, float("nan"), dtype=out_dt, device=dev())
-        B.ns_orthogonalize_noalloc(Xt, out, 5)
+        want = to_np(ref)
+        # two calls back to back on the same input: the second starts from the
+        # first call's leftovers in the shared scratch
+        outs = [torch.full(shape, float("nan"), dtype=out_dt, device=dev()) for _ in range(2)]
+        for out in outs:
+            B.ns_orthogonalize_noalloc(Xt, out, 5)
         torch.cuda.synchronize()
-        got, want = to_np(out), to_np(ref)
-        assert np.all(np.isfinite(got))
-        assert rel_fro(got, want) < NS_BF16_TOL
-        assert rel_fro(got, om.newton_schulz(to_np(Xt))) < NS_BF16_TOL
+        for out in outs:
+            got = to_np(out)
+            assert np.all(np.isfinite(got))
+            assert rel_fro(got, want) < NS_BF16_TOL
+            assert rel_fro(got, om.newton_schulz(to_np(Xt))) < NS_BF16_TOL
 
 
 def test_noalloc_rejects_a_matrix_beyond_the_scratch():
