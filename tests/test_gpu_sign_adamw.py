@@ -206,7 +206,7 @@ def test_int8_and_packed_votes_agree_on_gpu():
 
 
 @pytest.mark.parametrize("shape,ld", [((64, 64), None), ((5, 40), 48), ((33, 95), 96), ((2048, 2048), None),
-                                      ((64, 128), None), ((256, 512), None)])
+                                      ((64, 128), None), ((64, 192), None), ((256, 512), None)])
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_sign_pack_batched_bit_exact(shape, ld, M):
     Us = [_signed_input(shape, 100 + m) for m in range(M)]
