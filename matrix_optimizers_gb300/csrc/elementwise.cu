@@ -10,6 +10,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -22,17 +25,24 @@ namespace {
 // streaming kernels are sized to a single resident wave.
 template <typename K>
 int resident_blocks_per_sm(K kernel, int threads) {
-    static std::atomic<int> cache[64];
+    // keyed by the kernel itself: kernels of one signature share a pointer type
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, int>, int> cache;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
-    int v = cache[dev & 63].load();
-    if (v > 0) return v;
+    const auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), dev, threads);
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = 1;
     }
-    cache[dev & 63].store(n);
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = n;
     return n;
 }
 }  // namespace
