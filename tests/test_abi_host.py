@@ -192,3 +192,14 @@ def test_debug_view_dependency_counters():
     prev = B.mo_debug_set_ns_fused(0)
     assert B.mo_debug_set_ns_fused(2) == 0
     assert B.mo_debug_set_ns_fused(prev) == 2
+
+
+def test_missing_library_raises_instead_of_falling_back(monkeypatch, tmp_path):
+    # with no built library every entry point must fail loudly: there is no
+    # CPU or PyTorch fallback behind the binding
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "library_path", lambda: str(tmp_path / "libmatrixopt.so"))
+    with pytest.raises(ImportError):
+        B.load()
+    with pytest.raises(ImportError):
+        B.plan_owners([(64, 64), (128, 64)], 2, 5)
