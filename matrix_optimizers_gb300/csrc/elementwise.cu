@@ -124,7 +124,7 @@ __device__ __forceinline__ int64_t xop_offset(const MatDesc& md, bool fp32, int 
 // ------------------------------------------------------------ momentum_norm
 // Tile of 64 x 64 user elements per iteration, 256 threads: thread t owns
 // columns 4*(t%16)..+3 of rows t/16 + 16q, q = 0..3.
-__global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
+__global__ void __launch_bounds__(256, 8) momentum_norm_kernel(MomLaunch p) {
     __shared__ float tileT[kMomTile][kMomTile + 1];
     __shared__ float red[8];
     const int col4 = threadIdx.x & 15, rsub = threadIdx.x >> 4;
@@ -177,7 +177,32 @@ __global__ void __launch_bounds__(256) momentum_norm_kernel(MomLaunch p) {
             const int dt = op_dt;
             const int xr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;
             const int orow = c0 + xr;
-            if (orow < md.cols) {
+            if (orow < md.cols && !p.fp32_operand) {
+                // bf16 operand in 8-column blocks: each thread writes whole
+                // 16-byte runs (8 consecutive oriented columns of one row), so
+                // a warp stores four full 128-byte lines per instruction
+#pragma unroll
+                for (int g8 = 0; g8 < 2; ++g8) {
+                    const int ocol = r0 + seg + 8 * g8;
+                    const int nv = max(0, min(8, md.rows - ocol));
+                    if (nv > 0) {
+                        bf16* d = static_cast<bf16*>(dst) + xop_offset(md, false, orow, ocol);
+                        const float* v = &tileT[xr][seg + 8 * g8];
+                        if (nv == 8) {
+                            uint4 u;
+                            uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * q], v[2 * q + 1]);
+                                w[q] = *reinterpret_cast<uint32_t*>(&h);
+                            }
+                            *reinterpret_cast<uint4*>(d) = u;
+                        } else {
+                            for (int k = 0; k < nv; ++k) d[k] = __float2bfloat16_rn(v[k]);
+                        }
+                    }
+                }
+            } else if (orow < md.cols) {
 #pragma unroll
                 for (int g4 = 0; g4 < 4; ++g4) {
                     const int ocol = r0 + seg + 4 * g4;
