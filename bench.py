@@ -41,7 +41,7 @@ METRIC = "Muon step matrices/s and NS TFLOP/s (fraction of bf16 peak); vote GB/s
 # shape the kernel and its schedule hash to the value recorded with it.
 PROFILED_TRAFFIC = {
     ("llama7b_owner0", "fused"): {
-        "bytes_per_launch": 37.40e9 + 19.10e9,
+        "bytes_per_launch": 37.37e9 + 19.09e9,
         "sources_sha256": "0e71d6322b84d325bdf109ad92298a1dc95da8cd5bf1e8d3639605e8ca2d6e6c",
         "profile": "profiles/launches_llama7b_owner0.md",
     },
