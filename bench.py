@@ -28,41 +28,50 @@ import subprocess
 import sys
 import time
 
-import numpy as np
+# The CPU oracle's BLAS uses every core of this host: set before NumPy loads
+# (an explicit setting in the environment is kept), and recorded with the
+# CPU numbers.
+CORES = len(os.sched_getaffinity(0))
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(CORES))
+BLAS_THREADS = int(os.environ["OPENBLAS_NUM_THREADS"])
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "Muon step matrices/s and NS TFLOP/s (fraction of bf16 peak); vote GB/s vs HBM"
 
-
-# DRAM bytes (read + write) per launch of the NS kernel from one ncu capture
-# (profiles/launches_llama7b_owner0.md), valid only while the sources that
-# shape the kernel and its schedule hash to the value recorded with it.
-PROFILED_TRAFFIC = {
-    ("llama7b_owner0", "fused"): {
-        "bytes_per_launch": 37.37e9 + 19.09e9,
-        "sources_sha256": "0e71d6322b84d325bdf109ad92298a1dc95da8cd5bf1e8d3639605e8ca2d6e6c",
-        "profile": "profiles/launches_llama7b_owner0.md",
-    },
-}
+# DRAM bytes (read + write) per launch of the NS kernel, from an ncu capture
+# recorded in bench_traffic.json beside this file; valid only while the
+# sources that shape the kernel and its schedule hash to the value recorded
+# with it.
 TRAFFIC_SOURCES = ["matrix_optimizers_gb300/csrc/ns_tc.cu", "matrix_optimizers_gb300/csrc/ptx.cuh",
                    "matrix_optimizers_gb300/csrc/internal.h", "matrix_optimizers_gb300/csrc/api.cu"]
 
 
-def _profiled_traffic(workload, ns_launch, max_matrices, ns_tiles):
+def sources_sha256():
     import hashlib
-    rec = PROFILED_TRAFFIC.get((workload, ns_launch))
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def _profiled_traffic(workload, ns_launch, max_matrices, ns_tiles):
+    try:
+        with open(os.path.join(ROOT, "bench_traffic.json")) as f:
+            recs = json.load(f)
+    except (OSError, ValueError):
+        return None, "no traffic record"
+    rec = recs.get(f"{workload}/{ns_launch}")
     if rec is None or max_matrices or ns_tiles not in (None, "single"):
         return None, None
-    h = hashlib.sha256()
-    root = os.path.dirname(os.path.abspath(__file__))
-    for f in TRAFFIC_SOURCES:
-        with open(os.path.join(root, f), "rb") as fh:
-            h.update(fh.read())
-    if h.hexdigest() != rec["sources_sha256"]:
+    if rec["sources_sha256"] != sources_sha256():
         return None, "kernel sources changed since the ncu capture"
-    return rec["bytes_per_launch"], rec["profile"]
+    return rec["bytes_per_launch"], rec["capture"]
 
 
 def _peaks():
@@ -204,6 +213,21 @@ def _shape_summary(shapes):
     return " + ".join(f"{n}x{r}x{cc}" for (r, cc), n in c.items())
 
 
+def workload_config(workload, shapes, world):
+    """The `config` object of the JSON line: what the workload is (the same
+    for the GPU arm and the reference arm)."""
+    numel = sum(r * c for r, c in shapes)
+    state = (4 + 2 + 4) if workload == "sign_muon_m8" else (4 + 4 + 4)   # G, M, W bytes per element
+    return {
+        "workload": workload, "matrices_per_gpu": len(shapes), "shapes": _shape_summary(shapes),
+        "ns_steps": 5, "ns_coeffs": [3.4445, -4.7750, 2.0315],
+        "ns_flops_per_step_nominal": sum(ns_flops(s) for s in shapes),
+        "l2": f"inputs larger than L2: {numel * state / 1e9:.1f} GB of gradients, momentum and weights "
+              f"per GPU, no flush",
+        "parallelism": f"owner-sharded: each GPU steps one share of a {max(8, world)}-rank owner plan",
+    }
+
+
 def _max_over_ranks(x, dist):
     if dist is None:
         return x
@@ -333,13 +357,12 @@ def run_gb300(args, rank, world, local_rank, dist):
         "data": ("synthetic: 8 workers' gradients N(0,1) shared + N(0,0.5^2) per worker, bf16 momentum from 0, "
                  "N(0,0.02^2) shared W; step = fused sign-packed NS per worker + majority-vote update")
         if sign_muon else "synthetic: seeded N(0,0.02^2) weights, N(0,1e-3^2) gradients, zero initial momentum",
-        "config": {
-            "workload": args.workload, "matrices_per_gpu": len(shapes),
-            "shapes": _shape_summary(shapes), "ns_steps": 5, "ns_coeffs": [3.4445, -4.7750, 2.0315],
-            "ns_flops_per_step_nominal": flops_step, "ns_flops_per_step_issued": issued_step,
-            "l2": f"inputs larger than L2: {resident / 1e9:.1f} GB resident per GPU, no flush",
-            "parallelism": f"owner-sharded: each GPU steps one share of a {max(8, world)}-rank owner plan",
-            "precision": "bf16 tensor-core operands, fp32 accumulate / master / momentum",
+        "config": workload_config(args.workload, shapes, world),
+        "impl_config": {
+            "ns_flops_per_step_issued": issued_step,
+            "resident_gb": resident / 1e9,
+            "precision": ("bf16 tensor-core operands and NS iterate, fp32 accumulate, fp32 residual of the "
+                          "polynomial matrix's diagonal; fp32 momentum, weights and gradients"),
             "ns_launch": args.ns_launch,
             "ns_tiles": args.ns_tiles or "library default",
         },
@@ -352,6 +375,12 @@ def run_gb300(args, rank, world, local_rank, dist):
                        else "ns_tc_kernel, one fused launch of all Gram / polynomial / apply levels per step"),
             "bound": "tensor", "achieved": ns_tflops_kernel, "peak": sustained, "unit": "TFLOP/s",
             "frac": (ns_tflops_kernel / sustained) if ns_tflops_kernel else None,
+            # the MMA work the kernel issues (Gram and square on upper tiles only,
+            # about 0.7x nominal): the measure of tensor-pipe use
+            "issued_achieved": (issued_step * args.steps / (ns_ms * 1e-3) / 1e12) if ns_ms else None,
+            "issued_frac": (issued_step * args.steps / (ns_ms * 1e-3) / 1e12 / sustained) if ns_ms else None,
+            "issued_frac_of_burst": (issued_step * args.steps / (ns_ms * 1e-3) / 1e12 / peaks["bf16_tflops"])
+            if ns_ms else None,
             "peak_source": f"{peaks['source']} bf16 sustained (the kernel runs inside a long step)",
             "traffic": traffic, "traffic_source": traffic_src,
             "launches": ns_launches, "avg_launch_ms": ns_ms / max(1, ns_launches),
@@ -442,7 +471,7 @@ def run_gb300(args, rank, world, local_rank, dist):
         torch.cuda.synchronize()
         if dist is not None:
             dist.barrier()
-        k2 = max(1, min(args.steps, 5))
+        k2 = max(5, args.steps)
         e0.record(stream)
         for _ in range(k2):
             e2e_step()
@@ -610,7 +639,7 @@ def cpu_baseline(shapes_all, idx, budget_s=30.0):
     base = next(iter(per))
     t_set = sum((per[k] if k in per else per[base] * ns_flops(k) / ns_flops(base)) * len(classes[k])
                 for k in keys)
-    return {"value": len(idx) / t_set, "unit": "matrices/s", "cores": len(os.sched_getaffinity(0)),
+    return {"value": len(idx) / t_set, "unit": "matrices/s", "cores": CORES, "blas_threads": BLAS_THREADS,
             "kind": "oracle",
             "sample": f"one matrix for {len(per)} of {len(keys)} shape classes ({spent:.1f} s of fp64 NumPy); "
                       f"per-class times scaled by class counts (untimed classes by nominal flops) "
@@ -619,6 +648,12 @@ def cpu_baseline(shapes_all, idx, budget_s=30.0):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle as it stands, on the host cores.
+    Each step runs the whole owner step (momentum, NS, update) on ONE matrix
+    of the workload, cycling its shape classes; `ms_per_step` is the mean
+    measured time of those timed steps.  `value` estimates the oracle's
+    matrices/s on the workload's whole set from the per-class times, weighted
+    by the class counts (a class not timed is scaled by nominal flops)."""
     if rank != 0:
         return None
     from oracle import planner
@@ -627,12 +662,13 @@ def run_reference(args, rank, world):
     keys = sorted(classes)
     counted = {k: [] for k in keys}
     warm = {k: [] for k in keys}
+    timed = []
     for s in range(args.warmup + args.steps):
         k = keys[s % len(keys)]
         t = _oracle_matrix_time(shapes_all, classes[k][0])
         (counted if s >= args.warmup else warm)[k].append(t)
-    # a class not timed in the counted steps uses its warm-up time; one never
-    # timed at all is scaled from a timed class by nominal NS flops
+        if s >= args.warmup:
+            timed.append(t)
     per = {}
     for k in keys:
         if counted[k]:
@@ -645,16 +681,19 @@ def run_reference(args, rank, world):
             per[k] = per[base] * ns_flops(k) / ns_flops(base)
     t_set = sum(per[k] * len(classes[k]) for k in keys)
     value = len(idx) / t_set
-    cores = len(os.sched_getaffinity(0))
-    sample = (f"each step runs the fp64 oracle on one matrix, cycling the {len(keys)} shape classes; "
-              f"per-class mean times scaled by class counts of the {len(idx)}-matrix set")
+    sample = (f"each step runs the fp64 oracle's owner step on one matrix, cycling the {len(keys)} shape classes "
+              f"({args.steps} timed matrices); value = the {len(idx)}-matrix set's matrices/s from the per-class "
+              f"mean times weighted by class counts")
     return {"metric": METRIC, "value": value, "unit": "matrices/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_set * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs)",
-            "config": {"workload": args.workload, "matrices_per_gpu": len(idx)},
+            "warmup": args.warmup, "ms_per_step": float(np.mean(timed)) * 1e3 if timed else None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (the same seeded inputs as the GPU arm)",
+            "config": workload_config(args.workload, [shapes_all[i] for i in idx], world),
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "matrices/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "set_ms_estimate": t_set * 1e3,
+            "per_class_s": {f"{k[0]}x{k[1]}": per[k] for k in keys},
+            "cpu_baseline": {"value": value, "unit": "matrices/s", "cores": CORES, "blas_threads": BLAS_THREADS,
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "matrices/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -172,7 +172,14 @@ int ns_orthogonalize(const void* const* X, void* const* out,
  *     call's contents; calls whose work overlaps on the GPU (other streams,
  *     other threads) race and corrupt each other's results.
  *   - No cudaMalloc, cudaFree or other allocating routine is called.  The
- *     device error word is not exposed for this entry point.
+ *     device error word is not exposed for this entry point: a run whose
+ *     bounded device waits expire (about 2 s) leaves `out` unspecified and
+ *     still returns MO_OK.
+ *   - The call's small control block is copied from ordinary (pageable)
+ *     host memory with cudaMemcpyAsync, so the call may return only once
+ *     that copy has been staged: it is not fully asynchronous to the host.
+ *   - The looked-up device address is kept for the life of the process;
+ *     calls after a cudaDeviceReset on that device are not supported.
  * Arguments as ns_orthogonalize with n = 1 (X, out device pointers). */
 #define MO_NOALLOC_SCRATCH_BYTES (32u << 20)
 int ns_orthogonalize_noalloc(const void* X, void* out, int64_t rows, int64_t cols, int64_t ld,

@@ -22,12 +22,14 @@ extern "C" {
  *   bf16 mode: x_op[0], x_op[1] = bf16 m x n operand ping-pong in 8-column
  *              blocks: element (i, j) at byte ((j/8)*ldx + i)*16 + (j%8)*2,
  *              where ldx = m rounded up to 8 (X is kept in bf16 between
- *              steps, x_master = 0); gram = bf16 m x m row-major (lda),
- *              poly = bf16 m x m (lda).
- *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong (x_master = 0),
- *              gram, poly = fp32 m x m.
- * After a call with steps = 1 the gram buffer holds X0 X0^T and the poly
- * buffer b*A + c*A*A of that step.
+ *              steps); gram = bf16 m x m row-major (lda), poly = bf16 m x m
+ *              (lda); diag_res = m fp32 values, B_ii - bf16(B_ii) of the
+ *              polynomial matrix's diagonal, which the apply phase adds back
+ *              as a row scale of X.
+ *   fp32 mode: x_op[0], x_op[1] = fp32 m x n ping-pong, gram, poly = fp32
+ *              m x m; diag_res = 0 (unused).
+ * After a call with steps = 1 the gram buffer holds X0 X0^T, the poly buffer
+ * aI + b*A + c*A*A of that step (bf16) and diag_res its diagonal's residual.
  * deps: three int32 completion counters (Gram, polynomial, apply) of a fused
  * bf16 launch with per-matrix ordering; after such a call each holds
  * releases_per_tile x (that phase's tiles of this matrix: tiles_sym for Gram
@@ -39,7 +41,7 @@ extern "C" {
 typedef struct {
     int64_t m, n, ldx, lda;
     int32_t transposed, precision;
-    int64_t x_op[2], x_master, gram, poly;
+    int64_t x_op[2], diag_res, gram, poly;
     int64_t deps;
     int32_t tiles_sym, tiles_apply;
     int32_t releases_per_tile, reserved;
@@ -51,13 +53,6 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
 /* Number of SMs the grouped kernels size their grids for on the current
  * device (0 if no device). */
 int mo_debug_sm_count(void);
-
-/* Chooses between the two readings of the shared-memory descriptor strides
- * for the apply phase's MN-major operand (no swizzle: 8-row K groups 128 B
- * apart, 8-column MN blocks 1 KB apart): (lbo, sbo) = (128, 1024), the
- * default, or (1024, 128).  Other values give MO_ERR_INVALID_ARG.
- * Process-wide; affects launches issued after the call. */
-int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo);
 
 /* Chooses the tile geometry of the bf16 tensor-core Newton-Schulz kernel:
  * on = 1 runs 256 x 256 tiles on CTA pairs (clusters of 2, tcgen05
@@ -81,6 +76,20 @@ int mo_debug_set_ns_pair(int on);
  * MO_ERR_INVALID_ARG for a value outside 0..3.  Process-wide; affects calls
  * issued after it. */
 int mo_debug_set_ns_fused(int on);
+
+/* Failure-path test hook.  With matrix >= 0, every fused bf16 Newton-Schulz
+ * launch issued after the call makes the dependency waits of that matrix's
+ * tiles (index into the call's non-empty matrices; with grid-wide counters,
+ * every dependency wait of the launch) impossible to meet, and
+ * those launches' dependency waits give up after wait_cycles SM cycles
+ * (1000 .. 4e9; e.g. 2e6, about 1 ms) instead of about 2 s.  The wait then
+ * runs out, the launch unwinds (armed copies drained, issued MMAs drained,
+ * TMEM freed) and records MO_ERR_TIMEOUT for mo_check_device_status; the
+ * outputs of that call are unspecified.  matrix = -1 (the default) turns the
+ * hook off.  Per-phase launches have no dependency waits and are unaffected.
+ * Process-wide.  Returns MO_ERR_INVALID_ARG for matrix < -1 or a budget out
+ * of range. */
+int mo_debug_inject_dep_stall(int matrix, int64_t wait_cycles);
 
 /* SM load-balance record.  With a device buffer `buf` of
  * 4 * capacity * max_ctas uint64 values, each of the calling thread's next

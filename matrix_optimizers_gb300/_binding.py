@@ -54,7 +54,7 @@ class mo_adamw_tail(ctypes.Structure):
 class mo_ns_view(ctypes.Structure):
     _fields_ = [("m", c_int64), ("n", c_int64), ("ldx", c_int64), ("lda", c_int64),
                 ("transposed", c_int32), ("precision", c_int32),
-                ("x_op", c_int64 * 2), ("x_master", c_int64), ("gram", c_int64),
+                ("x_op", c_int64 * 2), ("diag_res", c_int64), ("gram", c_int64),
                 ("poly", c_int64), ("deps", c_int64), ("tiles_sym", c_int32), ("tiles_apply", c_int32),
                 ("releases_per_tile", c_int32), ("reserved", c_int32)]
 
@@ -97,8 +97,8 @@ _SIGNATURES = [
     ("mo_debug_ns_view", c_int32, [ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int32, c_int32,
                                    c_int32, ctypes.POINTER(mo_ns_view)]),
     ("mo_debug_sm_count", c_int32, []),
-    ("mo_debug_set_mn_strides", c_int32, [ctypes.c_uint32, ctypes.c_uint32]),
     ("mo_debug_set_ns_fused", c_int32, [c_int32]),
+    ("mo_debug_inject_dep_stall", c_int32, [c_int32, c_int64]),
     ("mo_debug_set_ns_pair", c_int32, [c_int32]),
     ("mo_debug_cta_stamps", c_int32, [c_void_p, c_int32, c_int32, ctypes.POINTER(c_int32)]),
     ("mo_trace_enable", c_int32, [c_int32]),
@@ -350,8 +350,10 @@ def mo_debug_ns_view(shapes, index, precision=MO_NS_BF16):
     return v
 
 
-def mo_debug_set_mn_strides(lbo, sbo):
-    _check(load().mo_debug_set_mn_strides(lbo, sbo))
+def mo_debug_inject_dep_stall(matrix, wait_cycles=2_000_000):
+    """Makes the fused NS launch's dependency waits of matrix `matrix` run out
+    after `wait_cycles` SM cycles (matrix -1 turns it off)."""
+    _check(load().mo_debug_inject_dep_stall(matrix, wait_cycles))
 
 
 def mo_debug_set_ns_pair(on):

@@ -82,9 +82,7 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
 
 // Descriptor strides of the apply phase's MN-major B operand (no swizzle:
 // 8-row K groups 128 B apart, 8-column MN blocks 1 KB apart), as (lbo, sbo).
-// Exposed to tests through the debug header.
-std::atomic<uint32_t> g_mn_lbo{128};
-std::atomic<uint32_t> g_mn_sbo{1024};
+constexpr uint32_t kMnLbo = 128, kMnSbo = 1024;
 // How the tensor-core iterations are launched: 1 one fused cooperative launch
 // (when the grid fits on the device at once) ordered by per-matrix counters;
 // 2 the same launch ordered by one grid-wide counter set; 3 (default) 1 when a
@@ -101,6 +99,10 @@ constexpr int64_t kPerMatrixDepsMaxSymTilesPerCta = 16;
 // workload; the single-CTA form is the default because its fused
 // (cooperative) launch can also be captured by the profiler.
 std::atomic<int> g_ns_pair{0};
+// Failure-path test hook: -1, or the matrix whose fused-launch dependency
+// waits can never be met, with the wait budget those launches then use.
+std::atomic<int> g_stall_mat{-1};
+std::atomic<long long> g_stall_wait_cycles{0};
 
 // Co-resident CTAs of the tensor-core kernel per device ordinal, queried once.
 std::mutex g_cap_mu;
@@ -191,7 +193,8 @@ struct Layout {
     int precision;
     size_t mats, tmaps, tiles[3], ranges[3], deps, partials, scales, power, bufs_begin, total;
     int64_t total_rows;            // sum of m (power-iteration rows)
-    std::vector<size_t> pv;        // per matrix: offset of its two power-iteration vectors
+    std::vector<size_t> pv;        // per matrix: offset of its two power-iteration vectors and its
+                                   // diagonal residual vector (3 x lda floats)
     size_t ctl_bytes;              // [0, ctl_bytes) is uploaded every call
     int64_t ntiles[3];
     int64_t mom_tiles;
@@ -246,7 +249,7 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
     L.total_rows = 0;
     for (size_t i = 0; i < n; ++i) {
         L.pv[i] = off;
-        off = align_up(off + 2 * static_cast<size_t>(L.shape[i].lda) * sizeof(float), 128);
+        off = align_up(off + 3 * static_cast<size_t>(L.shape[i].lda) * sizeof(float), 128);
         L.total_rows += L.shape[i].m;
     }
     off = align_up(off, kBufAlign);
@@ -456,6 +459,7 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
         d.scales = reinterpret_cast<float*>(base + L.scales) + kScaleStride * i;
         d.pv = reinterpret_cast<float*>(base + L.pv[i]);
         d.py = d.pv + s.lda;
+        d.dlo = d.pv + 2 * s.lda;
         d.row_begin = row_begin;
         row_begin += s.m;
         d.mom_tile_begin = mom_begin;
@@ -646,8 +650,10 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     np.c = o.c;
     np.alpha = o.alpha;
     np.decay = o.decay;
-    np.mn_lbo = g_mn_lbo.load();
-    np.mn_sbo = g_mn_sbo.load();
+    np.mn_lbo = kMnLbo;
+    np.mn_sbo = kMnSbo;
+    np.stall_mat = g_stall_mat.load();
+    np.dep_wait_cycles = np.stall_mat >= 0 ? g_stall_wait_cycles.load() : kDepWaitCycles;
     np.level_deps = reinterpret_cast<int*>(base + L.deps) + 4 * jobs.size();
     np.tot_sym = static_cast<int32_t>(plan->ntiles[kGram]);
     np.tot_apply = static_cast<int32_t>(plan->ntiles[kApply]);
@@ -1133,7 +1139,9 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
     view->precision = precision;
     view->x_op[0] = static_cast<int64_t>(b.x_op[0]);
     view->x_op[1] = static_cast<int64_t>(b.x_op[1]);
-    view->x_master = 0;                  // X is kept in bf16 only (the operand pair)
+    view->diag_res = precision == MO_NS_BF16
+                         ? static_cast<int64_t>(L.pv[active] + 2 * static_cast<size_t>(s.lda) * sizeof(float))
+                         : 0;
     view->gram = static_cast<int64_t>(b.gram);
     view->poly = static_cast<int64_t>(b.poly);
     view->deps = static_cast<int64_t>(L.deps + 4 * sizeof(int) * static_cast<size_t>(active));
@@ -1203,19 +1211,17 @@ int mo_debug_set_ns_pair(int on) {
     return g_ns_pair.exchange(on);
 }
 
+int mo_debug_inject_dep_stall(int matrix, int64_t wait_cycles) {
+    if (matrix < -1) return MO_ERR_INVALID_ARG;
+    if (matrix >= 0 && (wait_cycles < 1000 || wait_cycles > kDepWaitCycles)) return MO_ERR_INVALID_ARG;
+    g_stall_wait_cycles.store(matrix >= 0 ? wait_cycles : 0);
+    g_stall_mat.store(matrix);
+    return MO_OK;
+}
+
 int mo_debug_set_ns_fused(int on) {
     if (on < 0 || on > 3) return MO_ERR_INVALID_ARG;
     return g_ns_fused.exchange(on);
-}
-
-int mo_debug_set_mn_strides(uint32_t lbo, uint32_t sbo) {
-    // only the two readings of the no-swizzle MN-major layout; both keep every
-    // operand read inside the stage's B buffer
-    const bool ok = (lbo == 128u && sbo == 1024u) || (lbo == 1024u && sbo == 128u);
-    if (!ok) return MO_ERR_INVALID_ARG;
-    g_mn_lbo.store(lbo);
-    g_mn_sbo.store(sbo);
-    return MO_OK;
 }
 
 }  // extern "C"

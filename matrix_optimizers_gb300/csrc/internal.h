@@ -19,6 +19,9 @@ constexpr int kTcEpiWarps = 16;   // epilogue warps per CTA of the tensor-core k
 constexpr int kFpBM = 64, kFpBN = 64, kFpBK = 16;
 // Momentum / normalisation kernel tile.
 constexpr int kMomTile = 64;
+// SM cycles a fused launch's dependency wait spins before it gives up (about
+// 2 s at 2 GHz, as the kernels' other bounded waits).
+constexpr long long kDepWaitCycles = 4000000000LL;
 
 enum NsPhase : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
 
@@ -68,6 +71,8 @@ struct MatDesc {
                                // estimate (1 under Frobenius scaling); kScaleStride floats
     float* pv;                 // power-iteration vectors (m floats each)
     float* py;
+    float* dlo;                // m floats: B_ii - bf16(B_ii), the rounding residual of the polynomial
+                               // matrix's diagonal, added back by the apply epilogue
     int64_t row_begin;         // first global row of this matrix (power iteration)
     int64_t mom_tile_begin;    // first global index of this matrix's momentum tiles
     int32_t mom_tiles_r, mom_tiles_c;
@@ -108,6 +113,9 @@ struct NsLaunch {
     uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
     unsigned long long* stamps;  // null, or [4 * gridDim.x]: per CTA start / end %globaltimer (ns),
                                  // ns spent waiting on dependencies, number of waits that spun
+    long long dep_wait_cycles;   // SM cycles a dependency wait spins before it gives up
+    int32_t stall_mat;           // -1; else the dependency waits of this matrix's tiles can never be met
+                                 // (failure-path test: the wait runs out and reports MO_ERR_TIMEOUT)
 };
 
 struct MomLaunch {

@@ -4,6 +4,9 @@
 //   kGram   A = s * X X^T          (X: m x n bf16, K = n; s = 1/||M||_F^2 at step 0)
 //   kPoly   B = a*I + b*A + c * A A   (K = m; A is symmetric so A A = A A^T)
 //   kApply  X' = B X               (K = m; step 0: X' = B Xb / ||M||_F, Xb = bf16(M))
+//           + d_i X(i, j), d_i = B_ii - bf16(B_ii): the bf16 rounding of B's
+//           diagonal (values near a = 3.44) is the largest error of the step,
+//           so the polynomial epilogue keeps its fp32 residual per row
 //           the last step writes W <- W - lr*wd*W - lr*scale*X' (or the output)
 // kGram and kPoly compute only the 128 x 256 tiles that meet the upper
 // triangle (j >= i) and store each upper element at (i, j) and (j, i).
@@ -309,6 +312,15 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
         const float cs = step == 0 ? p.c * md.scales[3] : p.c;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = fmaf(cs, v[k], bs * a[k]) + (j0 + k == i ? p.a : 0.f);
+        if (i >= j0 && i < j0 + nv) {
+            // the diagonal lies near a = 3.44, where the bf16 spacing is 2^-6:
+            // keep its rounding residual (exact in fp32) for the apply epilogue
+            float dv = 0.f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (j0 + k == i) dv = v[k];
+            md.dlo[i] = dv - __bfloat162float(__float2bfloat16_rn(dv));
+        }
     }
     const int64_t row = static_cast<int64_t>(i) * md.lda;
     if (j0 >= i) {
@@ -359,6 +371,23 @@ __device__ __forceinline__ void epi_sign_pack(const MatDesc& md, int i, bool row
     }
 }
 
+// The apply epilogue's share of the diagonal correction: the lane's 32
+// operand elements X(i, j0 .. j0+31) (4 x 8-column blocks) and the residual
+// d_i of B's diagonal.  Both were written by other CTAs of the launch: read
+// at L2.
+__device__ __forceinline__ void load_diag_fix(const MatDesc& md, int step, int i, bool row_ok, int j0, uint4 (&xr)[4],
+                                              float& di) {
+    di = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xr[q] = make_uint4(0, 0, 0, 0);
+    if (!row_ok || j0 >= md.n) return;
+    di = __ldcg(md.dlo + i);
+    const uint4* src = static_cast<const uint4*>(md.x_op[step & 1]) + static_cast<int64_t>(j0 >> 3) * md.xrows + i;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (j0 + 8 * q < md.n) xr[q] = __ldcg(src + static_cast<int64_t>(q) * md.xrows);
+}
+
 // Called by all 32 lanes of a warp (the fused pack takes warp ballots);
 // lanes whose row lies beyond the matrix touch no memory.
 __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int step, int i, bool row_ok,
@@ -366,12 +395,21 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     const int n = md.n;
     if (j0 >= n) return;
     const int nv = row_ok ? min(32, n - j0) : 0;
-    float x[32];
+    uint4 xr[4];
+    float di;
+    load_diag_fix(md, step, i, row_ok, j0, xr, di);
+    float (&x)[32] = v;
     // X' = (aI + bA + cA^2) X is the accumulator (the polynomial phase put a
-    // on B's diagonal); step 0 multiplied the unscaled bf16(M), so it scales.
+    // on B's diagonal), plus d_i X(i, j) for the diagonal's bf16 residual;
+    // step 0 multiplied the unscaled bf16(M), so it scales.
     const float scale = step == 0 ? md.scales[0] * md.scales[4] : 1.f;   // 1/||M||_F (x 1/sigma_hat)
 #pragma unroll
-    for (int k = 0; k < 32; ++k) x[k] = scale * v[k];
+    for (int q = 0; q < 4; ++q) {
+        float xo[8];
+        unpack_bf16x8(xr[q], xo);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) x[8 * q + r] = scale * fmaf(di, xo[r], v[8 * q + r]);
+    }
     if (step + 1 < p.steps) {
         // the next operand, in 8-column blocks: the warp's 32 rows of one block
         // are 512 contiguous bytes (columns past n hold the accumulator's zeros)
@@ -459,9 +497,10 @@ __device__ __forceinline__ int dep_need(const NsLaunch& p, const Deps& d, int ph
 
 // Returns 1 when the dependencies were already met, 2 after spinning, 0 on
 // timeout / abort; *waited_ns accumulates the time spent spinning.
-__device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, int step, volatile int* abort_flag,
-                                      unsigned long long* waited_ns) {
-    const int need_g = dep_need(p, d, kGram, ph == kGram ? step - 1 : step);
+__device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, int step, bool stall,
+                                      volatile int* abort_flag, unsigned long long* waited_ns) {
+    // a stalled matrix needs far more releases than a launch can give
+    const int need_g = dep_need(p, d, kGram, ph == kGram ? step - 1 : step) + (stall ? (1 << 30) : 0);
     const int need_p = dep_need(p, d, kPoly, ph == kApply ? step : step - 1);
     const int need_a = dep_need(p, d, kApply, step - 1);
     long long t0 = 0;
@@ -483,7 +522,7 @@ __device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, 
             *abort_flag = 1;
             return 0;
         }
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > p.dep_wait_cycles) {
             *abort_flag = 1;
             atomicCAS(p.err, 0, 0x105);
             return 0;
@@ -517,6 +556,9 @@ __device__ __forceinline__ int2 unit_tiles(const NsLaunch& p, int ph, int unit) 
 }  // namespace
 
 
+// 576 threads are 18 warps, so one of the SM's four sub-partitions holds 5
+// of them: its 16 K registers cap a thread at 96 (a larger per-kernel cap
+// leaves the block unlaunchable).
 template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constant__ NsLaunch p) {
     using G = Geo<kPair>;
@@ -577,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     const MatDesc& md = p.mats[td.mat];
                     const int key = p.deps == 2 ? 0 : td.mat;
                     if (p.deps && key != dep_key) {
-                        const int w = wait_deps(p, deps_of(p, md), ph, step, abort_flag, &dep_wait_ns);
+                        // (grid-wide counters serve every matrix: there every wait stalls)
+                        const bool stall = p.stall_mat >= 0 && (td.mat == p.stall_mat || p.deps == 2);
+                        const int w = wait_deps(p, deps_of(p, md), ph, step, stall, abort_flag, &dep_wait_ns);
                         if (w == 0) { ok = false; break; }
                         dep_spins += w == 2;
                         fence_proxy_async_global();
@@ -642,22 +686,25 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 p.stamps[4 * blockIdx.x + 2] = dep_wait_ns;
                 p.stamps[4 * blockIdx.x + 3] = dep_spins;
             }
-            if (!ok) {
-                if (leader) {
-                    // let every armed copy land before the CTA exits
-                    for (int s = 0; s < G::kStages; ++s) {
-                        if (armed[s] == 0) continue;
-                        const uint32_t full = smem_u32(&ctl->full[s]);
-                        const uint32_t par = (armed[s] - 1u) & 1u;
-                        long long t0 = clock64();
-                        while (!mbar_try_wait(full, par) && clock64() - t0 < kWaitCycles) {}
-                    }
-                } else {
-                    // the peer's copies complete on the leader's barriers: give
-                    // those in flight time to land (far above a copy's latency)
+            if (leader) {
+                // every armed copy lands before the CTA exits, also when the MMA
+                // warp gave up before consuming them (a no-op when it consumed
+                // them all); in a pair the leader's barriers also count the
+                // peer's copies of the stages it armed
+                for (int s = 0; s < G::kStages; ++s) {
+                    if (armed[s] == 0) continue;
+                    const uint32_t full = smem_u32(&ctl->full[s]);
+                    const uint32_t par = (armed[s] - 1u) & 1u;
                     long long t0 = clock64();
-                    while (clock64() - t0 < (1LL << 22)) {}
+                    while (!mbar_try_wait(full, par) && clock64() - t0 < kWaitCycles) {}
                 }
+            } else if (!ok) {
+                // the peer cannot wait on the leader's barriers, which its copies
+                // complete on: give those in flight time to land (~2 ms, far
+                // above a copy's latency); the closing cluster barrier keeps
+                // this CTA's shared memory alive until the leader has drained
+                long long t0 = clock64();
+                while (clock64() - t0 < (1LL << 22)) {}
             }
         }
     } else if (warp == kMmaWarp) {
@@ -768,9 +815,18 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }          // warp-uniform exit
                 tc_fence_after();
-                if (p.deps && ph == kPoly) {
-                    // the Gram entries read below were released by other CTAs
-                    if (lane == 0) (void)ld_acquire_gpu(deps_of(p, md).cnt + kGram);
+                if (p.deps && ph != kGram) {
+                    // the Gram entries (poly), or the operand and B's diagonal
+                    // residual (apply), read below were released by other CTAs
+                    if (lane == 0) {
+                        const int* cnt = deps_of(p, md).cnt;
+                        if (ph == kPoly) {
+                            (void)ld_acquire_gpu(cnt + kGram);
+                        } else {
+                            (void)ld_acquire_gpu(cnt + kPoly);
+                            (void)ld_acquire_gpu(cnt + kApply);
+                        }
+                    }
                     __syncwarp();
                 }
                 const int i = td.ti * G::kTileRows + static_cast<int>(rank) * kTcBM + quarter * 32 + lane;
@@ -778,6 +834,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
 #pragma unroll 1
                 for (int ch = 0; ch < kEpiSliceCols / 32; ++ch) {
                     const int col = slice * kEpiSliceCols + ch * 32;
+                    const int j0 = td.tj * kTcBN + col;
                     uint32_t r[32];
                     __syncwarp();
                     tmem_ld_32x32b_x32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -787,7 +844,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     float v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-                    const int j0 = td.tj * kTcBN + col;
                     if (ph == kApply)
                         epi_apply(p, md, step, i, row_ok, j0, v);
                     else if (row_ok)

@@ -152,22 +152,25 @@ def test_sign_call_validation_without_device(lib):
 
 def test_debug_view_offsets_are_disjoint():
     shapes = [(100, 300), (300, 100), (64, 64)]
-    spans = []
+    spans, res = [], []
     for i in range(3):
         v = B.mo_debug_ns_view(shapes, i)
         assert (v.m, v.n) == ((100, 300) if i < 2 else (64, 64))
         assert v.transposed == (1 if i == 1 else 0)
         assert v.ldx % 8 == 0 and v.ldx >= v.m and v.lda % 64 == 0     # bf16 operand: 8-column blocks
         xb = -(-v.n // 8) * v.ldx * 16
-        assert v.x_master == 0                                # X stays in bf16 between steps
         spans += [(v.x_op[0], xb), (v.x_op[1], xb),
                   (v.gram, v.m * v.lda * 2), (v.poly, v.m * v.lda * 2)]
+        res.append((v.diag_res, v.m * 4))
     spans.sort()
     for (a, la), (b, _) in zip(spans, spans[1:]):
         assert a + la <= b and a % 1024 == 0
     assert spans[-1][0] + spans[-1][1] <= B.ns_workspace_bytes(shapes)
-    with pytest.raises(B.MoError):
-        B.mo_debug_set_mn_strides(4096, 4096)
+    # the diagonal residual vectors: disjoint, ahead of the NS buffers
+    res.sort()
+    for (a, la), (b, _) in zip(res, res[1:]):
+        assert a + la <= b and a % 128 == 0
+    assert res[-1][0] + res[-1][1] <= spans[0][0]
 
 
 def test_debug_view_dependency_counters():

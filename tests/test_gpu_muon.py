@@ -9,7 +9,6 @@ from oracle import adamw as oa
 from oracle import muon as om
 from oracle import planner as oplan
 from oracle import sign as osg
-from tests.ns_rounding_model import model_rel_err
 from tests.gpu_helpers import (MOM_TOL, NS_BF16_SPECTRAL_TOL, NS_BF16_TOL, NS_FP32_TOL, dev, rel_fro, to_dev,
                                to_np, workspace)
 from workloads import (CONFIGS, llama7b_shapes, matrix_inputs, matrix_set_inputs, ragged_shapes,
@@ -89,12 +88,7 @@ def test_many_tiny_matrices_one_step():
     cfg = mo.make_cfg(mu=0.95, lr=0.02)
     Ws, _ = _run(inputs, cfg)
     for w, inp in zip(Ws, inputs):
-        # M1 = G here (M0 = 0).  For m of 32 to 48 with a tight spectrum, bf16
-        # NS itself lands just above 2e-2 (the rounding model reaches 2.26e-2
-        # on 32 x 240), so each matrix's bound is the larger of 2e-2 and 1.5x
-        # the model's error for it
-        tol = max(NS_BF16_TOL, 1.5 * model_rel_err(inp["G"].astype(np.float32).astype(np.float64)))
-        _check_update(w, inp, 0.95, 0.02, tol)
+        _check_update(w, inp, 0.95, 0.02, NS_BF16_TOL)
 
 
 def test_weight_decay_and_update_scale():
@@ -181,8 +175,10 @@ def test_sign_muon_m8_step_bit_exact_vote():
 @pytest.mark.parametrize("shapes", [[(256, 512), (512, 256)], [(96, 160), (160, 96), (2048, 2048)],
                                     [(200, 64), (64, 224), (320, 320)]])
 def test_sign_packed_step_equals_separate_pack(shapes):
-    """Fused sign + pack in the last NS epilogue == sign_pack of the bf16
-    direction written by the unfused step, bit for bit."""
+    """Fused sign + pack in the last NS epilogue: bit for bit the oracle's
+    packing (sign(0) = +1, bit j % 32 of word j / 32) of the bf16 direction
+    that the unfused step writes, that direction within the NS bound of the
+    oracle's, and equal to sign_pack of it."""
     rng = np.random.default_rng(len(shapes))
     G = [rng.standard_normal(s).astype(np.float32) for s in shapes]
     cfg_out = mo.make_cfg(mu=0.95, apply_update=False, out_dtype=mo.MO_BF16)
@@ -207,6 +203,11 @@ def test_sign_packed_step_equals_separate_pack(shapes):
         assert torch.equal(a, b), s
     for m1, m2 in zip(Ms, Ms2):
         assert torch.equal(m1, m2)                       # same momentum state update
+    for a, u, g in zip(fused, U, G):
+        assert np.array_equal(a.cpu().numpy().view(np.uint32), osg.pack_bits(to_np(u)))
+        _, _, O = om.muon_step(np.zeros(g.shape), np.zeros(g.shape), g, mu=0.95, lr=0.02, m_dtype="bf16",
+                               apply_update=False)
+        assert rel_fro(to_np(u), O) < NS_BF16_TOL
 
 
 def test_sign_packed_step_rejects_unaligned_columns():
@@ -246,10 +247,13 @@ def test_llama7b_owner0_sampled():
     inputs = matrix_set_inputs(shapes, mine)
     cfg = mo.make_cfg(mu=c["mu"], lr=c["lr"])
     Ws, Ms = _run(inputs, cfg)
-    sq = next(k for k, i in enumerate(mine) if shapes[i][0] == shapes[i][1])
-    rect = next(k for k, i in enumerate(mine) if shapes[i][0] > shapes[i][1])
-    for k in (sq, rect):
-        _check_update(Ws[k], inputs[k], c["mu"], c["lr"], NS_BF16_TOL)
+    # elementwise against the oracle: the first and the last matrix of each
+    # shape class (4096 x 4096; 4096 x 11008 as is; 11008 x 4096 transposed)
+    classes = [lambda s: s[0] == s[1], lambda s: s[0] < s[1], lambda s: s[0] > s[1]]
+    for cls in classes:
+        ks = [k for k, i in enumerate(mine) if cls(shapes[i])]
+        for k in (ks[0], ks[-1]):
+            _check_update(Ws[k], inputs[k], c["mu"], c["lr"], NS_BF16_TOL)
     # every matrix: the update is finite and its Frobenius norm lies in the
     # NS band: ||O||_F^2 = sum sigma_i^2 with each sigma in [0.68, 1.21]
     for k, i in enumerate(mine):
@@ -261,6 +265,20 @@ def test_llama7b_owner0_sampled():
 
 
 @pytest.mark.slow
+def test_ns_8192_square_vs_oracle():
+    """The largest matrix the workloads draw, alone: 8192 x 8192 (128 K-blocks
+    in every phase, 64 x 32 apply tiles), elementwise against the oracle."""
+    X = np.random.default_rng(81).standard_normal((8192, 8192), dtype=np.float32)
+    Xt = torch.from_numpy(X).to(dev())
+    out = torch.zeros_like(Xt)
+    ws = workspace(mo.ns_workspace_bytes([(8192, 8192)]))
+    mo.ns_orthogonalize([Xt], [out], 5, ws)
+    torch.cuda.synchronize()
+    assert mo.mo_check_device_status(ws) == 0
+    assert rel_fro(to_np(out), om.newton_schulz(X.astype(np.float64))) < NS_BF16_TOL
+
+
+@pytest.mark.slow
 def test_ragged500_sampled():
     c = CONFIGS["ragged500"]
     shapes = ragged_shapes()
@@ -268,9 +286,11 @@ def test_ragged500_sampled():
     cfg = mo.make_cfg(mu=c["mu"], lr=c["lr"])
     Ws, _ = _run(inputs, cfg)
     sizes = [r * cc for r, cc in shapes]
-    picks = {int(np.argmin(sizes)), int(np.argmax([min(s) for s in shapes])), 17, 250, 499}
-    picks = [k for k in picks if min(shapes[k]) <= 4096]
-    for k in picks:
+    # the smallest matrix, the one with the largest m (about 8000: 125 Gram
+    # K-blocks of 64 and 63 apply row tiles), the largest, and three more
+    picks = {int(np.argmin(sizes)), int(np.argmax([min(s) for s in shapes])), int(np.argmax(sizes)), 17, 250, 499}
+    assert max(min(shapes[k]) for k in picks) > 4096
+    for k in sorted(picks):
         _check_update(Ws[k], inputs[k], c["mu"], c["lr"], NS_BF16_TOL)
     for k in range(len(shapes)):
         d = (to_np(Ws[k]) - inputs[k]["W"]) / c["lr"]

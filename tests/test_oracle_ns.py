@@ -201,6 +201,35 @@ def test_muon_step_composes_momentum_ns_update():
     assert np.array_equal(W2, W)
 
 
+def test_muon_update_pins():
+    """The update against facts its formula does not restate.
+    * Descent: for a linear loss <G, W> and mu = 0, the step changes the loss
+      by -lr * s * <G, O> = -lr * s * sum_i sigma_i p^5(sigma_i / ||G||_F),
+      computed here from the singular values of G alone (negative: a wrong
+      sign, scale or operand of the update fails).
+    * Decoupled decay: a zero gradient gives a zero direction, so the step
+      only shrinks W by the factor (1 - lr * wd), and leaves it as is at wd = 0.
+    * Size: the step's spectral norm over lr * s lies in the NS output band."""
+    rng = np.random.default_rng(17)
+    W, G = rng.standard_normal((12, 30)), rng.standard_normal((12, 30))
+    lr, s = 0.02, 1.5
+    W1, _, _ = om.muon_step(W, np.zeros_like(W), G, mu=0.0, lr=lr, update_scale=s)
+    sv = np.linalg.svd(G, compute_uv=False)
+    q = sv / np.linalg.norm(G)
+    for _ in range(5):
+        q = _p(q)
+    want = -lr * s * float(np.sum(sv * q))
+    assert want < 0
+    np.testing.assert_allclose(float(np.sum(G * (W1 - W))), want, rtol=1e-10)
+    Z = np.zeros_like(G)
+    Wd, _, _ = om.muon_step(W, Z, Z, mu=0.9, lr=lr, weight_decay=0.3)
+    np.testing.assert_allclose(Wd, (1 - lr * 0.3) * W, rtol=1e-15)
+    W0, _, _ = om.muon_step(W, Z, Z, mu=0.9, lr=lr)
+    assert np.array_equal(W0, W)
+    step_norm = np.linalg.norm(W1 - W, 2) / (lr * s)
+    assert 0.68 < step_norm < 1.2024
+
+
 def test_ns_flops_count():
     assert om.ns_flops(4096, 4096) == 5 * 6 * 4096 ** 3
     assert om.ns_flops(11008, 4096) == om.ns_flops(4096, 11008) == \

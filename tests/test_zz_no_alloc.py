@@ -40,9 +40,14 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         # two calls back to back on the same input: the second starts from the
         # first call's leftovers in the shared scratch
         outs = [torch.full(shape, float("nan"), dtype=out_dt, device=dev()) for _ in range(2)]
-        for out in outs:
-            B.ns_orthogonalize_noalloc(Xt, out, 5)
+        B.ns_orthogonalize_noalloc(Xt, outs[0], 5)
         torch.cuda.synchronize()
+        free_after_first = torch.cuda.mem_get_info()[0]
+        B.ns_orthogonalize_noalloc(Xt, outs[1], 5)
+        torch.cuda.synchronize()
+        # the second call takes no device memory at all (the first may have
+        # loaded the library's module and its scratch array)
+        assert torch.cuda.mem_get_info()[0] == free_after_first
         for out in outs:
             got = to_np(out)
             assert np.all(np.isfinite(got))

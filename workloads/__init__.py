@@ -7,5 +7,6 @@ neither ``oracle`` nor ``matrix_optimizers_gb300``.
 from .configs import (  # noqa: F401
     NS_COEFFS, gpt_small_shapes, llama7b_shapes, ragged_shapes,
     matrix_inputs, matrix_set_inputs, sign_muon_inputs, tail_inputs, single_matrix_inputs,
+    tight_spectrum_matrix,
     CONFIGS,
 )

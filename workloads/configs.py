@@ -118,6 +118,17 @@ def sign_muon_inputs(workers=8, n=2048, seed_g=0, noise_std=0.5, seed_w=100):
     return {"G": grads, "W": W}
 
 
+def tight_spectrum_matrix(m, n, seed=0, spread=0.01):
+    """An m x n (m <= n) float32 matrix whose singular values all lie within
+    +-`spread` of 1: orthonormal rows (QR of an n x m N(0,1) draw from
+    default_rng(seed)) scaled per row by 1 + spread * N(0,1) (default_rng(seed + 9)).
+    Normalised by its Frobenius norm, every singular value starts near
+    1/sqrt(m): the hardest start for bf16 Newton-Schulz."""
+    Q, _ = np.linalg.qr(np.random.default_rng(seed).standard_normal((n, m)))
+    scale = 1.0 + spread * np.random.default_rng(seed + 9).standard_normal((m, 1))
+    return (Q.T * scale).astype(np.float32)
+
+
 def tail_inputs(numel, seed=7, w_std=0.02, g_std=1e-3):
     """AdamW tail: float32 W, g; m = v = 0."""
     return {
