@@ -298,8 +298,8 @@ def run_gb300(args, rank, world, local_rank, dist):
 
     def step():
         if sign_muon:
-            mo.muon_step_sign_packed(mats, cfg, words, ws)
-            mo.sign_vote_update(words, Wv, cfgd["lr"])
+            # one call: momentum, NS with the fused sign pack, then the vote
+            mo.muon_step_sign_vote(mats, cfg, words, Wv, cfgd["lr"], ws)
         else:
             mo.muon_step_batched(mats, cfg, ws, tail=tail)
 
@@ -355,7 +355,8 @@ def run_gb300(args, rank, world, local_rank, dist):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": ("synthetic: 8 workers' gradients N(0,1) shared + N(0,0.5^2) per worker, bf16 momentum from 0, "
-                 "N(0,0.02^2) shared W; step = fused sign-packed NS per worker + majority-vote update")
+                 "N(0,0.02^2) shared W; step = one muon_step_sign_vote call: per-worker momentum and NS with the "
+                 "sign pack fused into the last epilogue, then the majority-vote update")
         if sign_muon else "synthetic: seeded N(0,0.02^2) weights, N(0,1e-3^2) gradients, zero initial momentum",
         "config": workload_config(args.workload, shapes, world),
         "impl_config": {

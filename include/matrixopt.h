@@ -138,6 +138,21 @@ int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg,
 int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg,
                           uint32_t* const* words, void* ws, size_t ws_bytes, mo_stream_t stream);
 
+/* The whole Sign-Muon step of one GPU that holds the M workers (SignMuon §2
+ * "Flusso Algoritmico" steps 1-4, "Meccanismo Principale" 3): each worker's
+ * momentum, NS and fused sign + 1-bit pack as muon_step_sign_packed (mats[i]
+ * is worker i, words[i] receives its packed signs), then the majority vote
+ * over the M = n packed buffers and W <- W - lr*vote as sign_vote_update.
+ * Every worker has the same rows x cols (cols a multiple of 32); W is
+ * rows x cols with leading dimension ld (>= cols), MO_F32 or MO_BF16, element
+ * alignment; 1 <= M <= 128 non-empty workers (else MO_ERR_INVALID_ARG or
+ * MO_ERR_UNSUPPORTED).  Two launches on `stream`: the NS with the fused pack,
+ * then the vote.  W and the words equal those of muon_step_sign_packed +
+ * sign_vote_update.  ws sized by mo_workspace_bytes. */
+int muon_step_sign_vote(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, uint32_t* const* words,
+                        void* W, int w_dtype, int64_t ld, float lr, void* ws, size_t ws_bytes,
+                        mo_stream_t stream);
+
 /* Workspace size for ns_orthogonalize on these shapes (host only). */
 int ns_workspace_bytes(const int64_t* rows, const int64_t* cols, int n,
                        int precision, size_t* bytes_out);

@@ -68,6 +68,9 @@ _SIGNATURES = [
                                     c_void_p, c_size_t, c_void_p]),
     ("muon_step_sign_packed", c_int32, [ctypes.POINTER(mo_matrix), c_int32, ctypes.POINTER(mo_muon_cfg),
                                         ctypes.POINTER(c_void_p), c_void_p, c_size_t, c_void_p]),
+    ("muon_step_sign_vote", c_int32, [ctypes.POINTER(mo_matrix), c_int32, ctypes.POINTER(mo_muon_cfg),
+                                      ctypes.POINTER(c_void_p), c_void_p, c_int32, c_int64, c_float, c_void_p,
+                                      c_size_t, c_void_p]),
     ("ns_workspace_bytes", c_int32, [ctypes.POINTER(c_int64), ctypes.POINTER(c_int64), c_int32, c_int32,
                                      ctypes.POINTER(c_size_t)]),
     ("ns_orthogonalize", c_int32, [ctypes.POINTER(c_void_p), ctypes.POINTER(c_void_p),
@@ -226,6 +229,15 @@ def muon_step_sign_packed(mats, cfg, words, ws, stream=None):
     arr = (c_void_p * max(1, len(words)))(*[w.data_ptr() for w in words])
     _check(load().muon_step_sign_packed(_mat_array(mats), len(mats), ctypes.byref(cfg), arr, _ptr(ws),
                                         ws.numel() if ws is not None else 0, _stream(stream)))
+
+
+def muon_step_sign_vote(mats, cfg, words, W, lr, ws, stream=None):
+    """The Sign-Muon step of the M workers ``mats``: momentum + NS with fused
+    sign packing into ``words``, then the majority vote W <- W - lr * vote."""
+    arr = (c_void_p * max(1, len(words)))(*[w.data_ptr() for w in words])
+    _check(load().muon_step_sign_vote(_mat_array(mats), len(mats), ctypes.byref(cfg), arr, _ptr(W),
+                                      dtype_code(W.dtype), _ld(W), lr, _ptr(ws),
+                                      ws.numel() if ws is not None else 0, _stream(stream)))
 
 
 def ns_workspace_bytes(shapes, precision=MO_NS_BF16):

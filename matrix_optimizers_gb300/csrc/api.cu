@@ -332,6 +332,12 @@ struct NsOpts {
     int precision, steps, apply_update;
     float mu, a, b, c, alpha, decay;
     int spectral_iters = 0;        // > 0: spectral-scale normalisation with this many power iterations
+    // Sign-Muon vote after the NS (muon_step_sign_vote): W <- W - lr * vote of
+    // the jobs' packed signs, a launch of its own after the NS
+    void* vote_W = nullptr;
+    int vote_w_dtype = MO_F32;
+    int64_t vote_ld = 0;
+    float vote_lr = 0.f;
 };
 
 // ------------------------------------------------------------ launch trace
@@ -715,6 +721,16 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
         }
         lv = lv1;
     }
+    if (o.vote_W != nullptr) {
+        // the Sign-Muon vote over the packed signs the last epilogue wrote
+        std::vector<const uint32_t*> wp;
+        for (const Job& j : jobs) wp.push_back(j.words);
+        e = traced(MO_K_VOTE, stream, [&] {
+            return launch_sign_vote_update(wp.data(), static_cast<int>(wp.size()), jobs[0].rows, jobs[0].cols,
+                                           o.vote_W, o.vote_w_dtype, o.vote_ld, o.vote_lr, stream);
+        });
+        if (e != cudaSuccess) return MO_ERR_CUDA;
+    }
     return MO_OK;
 }
 
@@ -833,13 +849,19 @@ int muon_step_batched(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, cons
     return run_ns(jobs, o, ws, ws_bytes, s);
 }
 
-int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, uint32_t* const* words, void* ws,
-                          size_t ws_bytes, mo_stream_t stream) {
+}  // extern "C"
+
+namespace mo {
+namespace {
+// The jobs of a Sign-Muon step with the sign + 1-bit pack fused into the last
+// NS epilogue: momentum and gradient buffers validated, packed-word targets
+// attached, no W update or output.
+int gather_sign_jobs(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, uint32_t* const* words,
+                     std::vector<Job>& jobs) {
     if (cfg == nullptr) return MO_ERR_INVALID_ARG;
     if (cfg->ns_precision != MO_NS_BF16 || cfg->ns_steps < 1) return MO_ERR_UNSUPPORTED;
     mo_muon_cfg c2 = *cfg;
     c2.apply_update = 0;
-    std::vector<Job> jobs;
     std::vector<int> idx;
     int st = gather_muon_jobs(mats, n, &c2, nullptr, false, jobs, &idx);
     if (st != MO_OK) return st;
@@ -856,6 +878,18 @@ int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, 
         jobs[k].W = nullptr;
         jobs[k].out = nullptr;
     }
+    return MO_OK;
+}
+}  // namespace
+}  // namespace mo
+
+extern "C" {
+
+int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, uint32_t* const* words, void* ws,
+                          size_t ws_bytes, mo_stream_t stream) {
+    std::vector<Job> jobs;
+    int st = gather_sign_jobs(mats, n, cfg, words, jobs);
+    if (st != MO_OK) return st;
     NsOpts o;
     o.precision = MO_NS_BF16;
     o.steps = cfg->ns_steps;
@@ -867,6 +901,35 @@ int muon_step_sign_packed(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, 
     o.alpha = 0.f;
     o.decay = 0.f;
     o.spectral_iters = cfg->spectral_iters;
+    return run_ns(jobs, o, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int muon_step_sign_vote(const mo_matrix* mats, int n, const mo_muon_cfg* cfg, uint32_t* const* words, void* W,
+                        int w_dtype, int64_t ld, float lr, void* ws, size_t ws_bytes, mo_stream_t stream) {
+    std::vector<Job> jobs;
+    int st = gather_sign_jobs(mats, n, cfg, words, jobs);
+    if (st != MO_OK) return st;
+    if (jobs.empty()) return MO_OK;
+    if (static_cast<int>(jobs.size()) > kMaxVoteWorkers) return MO_ERR_UNSUPPORTED;
+    for (const Job& j : jobs)
+        if (j.rows != jobs[0].rows || j.cols != jobs[0].cols) return MO_ERR_INVALID_ARG;
+    if (W == nullptr || !valid_dtype(w_dtype) || ld < jobs[0].cols) return MO_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) % elem_size(w_dtype)) != 0) return MO_ERR_ALIGNMENT;
+    NsOpts o;
+    o.precision = MO_NS_BF16;
+    o.steps = cfg->ns_steps;
+    o.apply_update = 0;
+    o.mu = cfg->mu;
+    o.a = cfg->a;
+    o.b = cfg->b;
+    o.c = cfg->c;
+    o.alpha = 0.f;
+    o.decay = 0.f;
+    o.spectral_iters = cfg->spectral_iters;
+    o.vote_W = W;
+    o.vote_w_dtype = w_dtype;
+    o.vote_ld = ld;
+    o.vote_lr = lr;
     return run_ns(jobs, o, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -22,6 +22,8 @@ constexpr int kMomTile = 64;
 // SM cycles a fused launch's dependency wait spins before it gives up (about
 // 2 s at 2 GHz, as the kernels' other bounded waits).
 constexpr long long kDepWaitCycles = 4000000000LL;
+// The most workers a vote counts over (8-bit bit-sliced counts).
+constexpr int kMaxVoteWorkers = 128;
 
 enum NsPhase : int32_t { kGram = 0, kPoly = 1, kApply = 2 };
 

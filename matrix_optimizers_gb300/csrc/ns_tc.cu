@@ -531,6 +531,9 @@ __device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, 
     }
 }
 
+// Gram tiles with at least this many K blocks alternate their K direction.
+constexpr int kReverseMinKBlocks = 64;
+
 // TMA loads of one box, the pair form counting on the leader's barrier.
 template <bool kPair>
 __device__ __forceinline__ void load2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y) {
@@ -644,9 +647,17 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     // one K loop per phase, chosen once per tile: the copies differ by
                     // phase, and any branch among them inside the loop measured ~20%
                     // slower in every phase (the producer's issue rate is on the
-                    // critical path)
+                    // critical path).  In the Gram phase with a long K, every other
+                    // tile of the CTA's list walks K backwards: the CTAs of one wave
+                    // stream the X panels' K slices together, so the next wave starts
+                    // on the slices the last one read most recently, still in L2
+                    // (walking one way each wave re-reads from DRAM what the wave
+                    // before evicted)
+                    const bool rev = ph == kGram && td.nkb >= kReverseMinKBlocks && (t & 1);
+                    const int k_last = rev ? td.nkb - 1 : 0;
+                    const int k_inc = rev ? -1 : 1;
                     auto k_loop = [&](auto&& load) {
-                        for (int kb = 0; kb < td.nkb; ++kb) {
+                        for (int kb = 0, kk = k_last; kb < td.nkb; ++kb, kk += k_inc) {
                             const uint32_t empty = smem_u32(&ctl->empty[stage]);
                             const uint32_t full = smem_u32(&ctl->full[stage]);
                             if (!mbar_wait_bounded(empty, phase ^ 1u, abort_flag, p.err, 0x101)) {
@@ -657,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                             ++armed[stage];
                             const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
                             const uint32_t bar = kPair ? mapa_shared(full, 0) : full;   // the leader's barrier
-                            load(sa, sa + kABytes, bar, kb * kTcBK);
+                            load(sa, sa + kABytes, bar, kk * kTcBK);
                             if (++stage == G::kStages) { stage = 0; phase ^= 1u; }
                         }
                     };

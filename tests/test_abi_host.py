@@ -131,6 +131,34 @@ def test_validation_errors_without_device(lib):
                                  None) == B.MO_ERR_ALIGNMENT
 
 
+def test_sign_vote_step_validation_without_device(lib):
+    cfg = B.make_cfg(apply_update=False)
+
+    def call(mats, W=256, w_dtype=0, ld=64, words=(256, 512)):
+        arr = (B.mo_matrix * len(mats))(*mats)
+        wp = (ctypes.c_void_p * len(words))(*words)
+        return lib.muon_step_sign_vote(arr, len(mats), ctypes.byref(cfg), wp, ctypes.c_void_p(W), w_dtype, ld,
+                                       1e-3, ctypes.c_void_p(1 << 20), 1 << 40, None)
+
+    a = B.mo_matrix(32, 64, 64, 0, 0, 0, 0, 256, 256, 256)
+    b = B.mo_matrix(64, 32, 32, 0, 0, 0, 0, 256, 256, 256)          # another shape
+    c = B.mo_matrix(32, 48, 48, 0, 0, 0, 0, 256, 256, 256)          # cols not a multiple of 32
+    assert call([a, b]) == B.MO_ERR_INVALID_ARG
+    assert call([c, c], ld=48) == B.MO_ERR_UNSUPPORTED
+    assert call([a, a], W=0) == B.MO_ERR_INVALID_ARG
+    assert call([a, a], ld=32) == B.MO_ERR_INVALID_ARG                # ld below cols
+    assert call([a, a], W=258) == B.MO_ERR_ALIGNMENT                  # fp32 W on a 2-byte boundary
+    assert call([a, a], words=(256, 0)) == B.MO_ERR_INVALID_ARG
+    assert call([a, a], words=(256, 514)) == B.MO_ERR_ALIGNMENT
+    fp32 = B.make_cfg(apply_update=False, precision=B.MO_NS_FP32)
+    arr = (B.mo_matrix * 1)(a)
+    wp = (ctypes.c_void_p * 1)(256)
+    assert lib.muon_step_sign_vote(arr, 1, ctypes.byref(fp32), wp, ctypes.c_void_p(256), 0, 64, 1e-3,
+                                   ctypes.c_void_p(1 << 20), 1 << 40, None) == B.MO_ERR_UNSUPPORTED
+    empty = (B.mo_matrix * 1)(B.mo_matrix(0, 64, 64, 0, 0, 0, 0, 0, 0, 0))
+    assert lib.muon_step_sign_vote(empty, 1, ctypes.byref(cfg), wp, None, 0, 64, 1e-3, None, 0, None) == B.MO_OK
+
+
 def test_sign_call_validation_without_device(lib):
     assert lib.sign_pack(None, 0, 4, 4, 4, None, None) == B.MO_ERR_INVALID_ARG
     assert lib.sign_pack(ctypes.c_void_p(256), 5, 4, 4, 4, ctypes.c_void_p(256), None) == B.MO_ERR_INVALID_ARG

@@ -1,7 +1,10 @@
 """The CTA-pair geometry of the NS kernel (256 x 256 tiles, tcgen05
 cta_group::2 across a cluster of two CTAs) against the single-CTA geometry
 (128 x 256 tiles) and the oracle, over ragged shapes, tails below one tile,
-transposed matrices and every output form."""
+transposed matrices and every output form.  The two geometries schedule
+different tiles and each walks K backwards on every other tile of a CTA's
+list, so their fp32 sums differ in order: they agree to accumulation noise,
+not bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -74,8 +77,12 @@ def test_pair_vs_single_and_oracle(case, fused):
             assert rel_fro(to_np(a), O) < tol, s
         else:
             assert rel_fro(to_np(a) - W0, Wn - W0) < tol, s
-        # the two geometries issue the same MMAs in the same K order
-        assert torch.equal(a, b), (s, _diff(a, b))
+        # the same products, summed in another K order
+        if kw.get("apply_update", True) is False:
+            assert _diff(a, b) < 2e-3, s
+        else:
+            W0t = torch.from_numpy(inp["W"]).to(dev())
+            assert _diff(a - W0t, b - W0t) < 2e-3, s
 
 
 def test_pair_sign_packed_equals_single():
@@ -98,5 +105,7 @@ def test_pair_sign_packed_equals_single():
             res.append(words)
         finally:
             B.mo_debug_set_ns_pair(prev)
+    # a sign can differ only where the two accumulation orders straddle zero
     for a, b, s in zip(res[0], res[1], shapes):
-        assert torch.equal(a, b), s
+        flips = int(torch.sum(torch.bitwise_xor(a, b) != 0).item())
+        assert flips <= max(2, a.numel() // 500), (s, flips)
