@@ -384,6 +384,11 @@ def run_gb300(args, rank, world, local_rank, dist):
             if ns_ms else None,
             "peak_source": f"{peaks['source']} bf16 sustained (the kernel runs inside a long step)",
             "traffic": traffic, "traffic_source": traffic_src,
+            # per NS step Gram reads X (2 B/elt) and writes A (2 B per m^2), the
+            # polynomial phase reads A and writes B, apply reads B and X and
+            # writes X; the last step writes no X but reads and writes fp32 W
+            "algorithmic_bytes_per_launch": None if sign_muon else
+            sum(5 * (6 * min(s) * max(s) + 8 * min(s) ** 2) + 6 * min(s) * max(s) for s in shapes),
             "launches": ns_launches, "avg_launch_ms": ns_ms / max(1, ns_launches),
             "work": "nominal 4m^2n+2m^3 flops per NS step per matrix",
         },
