@@ -426,11 +426,19 @@ def run_gb300(args, rank, world, local_rank, dist):
         n_auto = int(round((sum(g.numel() for g in hG) + sum(w.numel() for w in hW)) * 4 / 170e6))
         n_groups = max(1, min(args.e2e_groups if args.e2e_groups > 0 else max(2, min(8, n_auto)), len(shapes)))
         sizes = [r * c for r, c in shapes]
+        # group k's share of the bytes: even, or ramped (1, 2, 4, ... up to the
+        # middle and back down) so that the copy-in before the first kernel and
+        # the copy-out after the last one are short
+        if args.e2e_shape == "ramp":
+            half = [2.0 ** min(k, n_groups - 1 - k) for k in range(n_groups)]
+        else:
+            half = [1.0] * n_groups
+        bounds = np.cumsum(half) / sum(half) * sum(sizes)
         groups, cur, acc = [], [], 0
         for i, sz in enumerate(sizes):
             cur.append(i)
             acc += sz
-            if len(groups) < n_groups - 1 and acc >= sum(sizes) * (len(groups) + 1) / n_groups:
+            if len(groups) < n_groups - 1 and acc >= bounds[len(groups)]:
                 groups.append(cur)
                 cur = []
         if cur:
@@ -719,6 +727,8 @@ def main():
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="matrix groups of the end-to-end step (copies of one overlap the kernels of another); "
                          "0: one per ~170 MB of host traffic, 2 to 8")
+    ap.add_argument("--e2e-shape", default="even", choices=["even", "ramp"],
+                    help="byte shares of the end-to-end groups: equal, or small first and last groups")
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
