@@ -68,11 +68,13 @@ bool get_encode() {
     return g_encode != nullptr;
 }
 
-// bf16 rows x cols (leading dim ld elements), box 64 x 64, 128-byte swizzle.
-bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+// bf16 rows x cols (leading dim ld elements), box 64 columns x box_rows rows,
+// 128-byte swizzle: the box lands as box_rows contiguous 128-byte rows, the
+// same layout as box_rows / 64 stacked 64-row boxes, in one copy.
+bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
-    cuuint32_t box[2] = {64, 64};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -153,7 +155,7 @@ Shape oriented(int64_t rows, int64_t cols) {
 // (8 rows x 8 columns of one block, 128 contiguous bytes), row groups of 8,
 // column blocks.  A box of `rows` x `cols` of X lands in shared memory as
 // [column block][row][8 elements], the no-swizzle canonical layout.
-constexpr int kMapsPerMatrix = 8;    // 3 views of each operand buffer, Gram, polynomial
+constexpr int kMapsPerMatrix = 9;    // 3 views of each operand buffer, 2 of the Gram matrix, polynomial
 bool encode_xop_map(CUtensorMap* map, const void* base, const Shape& s, int rows, int cols) {
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(s.xrows / 8), static_cast<cuuint64_t>(s.xblocks)};
     cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(s.xrows * 16)};
@@ -488,13 +490,15 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
                 d.tm_xb[q] = dm0 + 3 * q + 1;
                 d.tm_xn[q] = dm0 + 3 * q + 2;
             }
-            if (!encode_bf16_map(&hm0[6], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
-            if (!encode_bf16_map(&hm0[7], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&hm0[6], d.gram, s.m, s.m, s.lda, kTcBM)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&hm0[7], d.gram, s.m, s.m, s.lda, bn)) return MO_ERR_CUDA;
+            if (!encode_bf16_map(&hm0[8], d.poly, s.m, s.m, s.lda, kTcBM)) return MO_ERR_CUDA;
             d.tm_gram = dm0 + 6;
-            d.tm_poly = dm0 + 7;
+            d.tm_gram_b = dm0 + 7;
+            d.tm_poly = dm0 + 8;
         } else {
             for (int q = 0; q < 2; ++q) d.tm_xa[q] = d.tm_xb[q] = d.tm_xn[q] = nullptr;
-            d.tm_gram = d.tm_poly = nullptr;
+            d.tm_gram = d.tm_gram_b = d.tm_poly = nullptr;
         }
     }
 

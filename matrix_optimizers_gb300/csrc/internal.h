@@ -66,8 +66,9 @@ struct MatDesc {
     const CUtensorMap* tm_xa[2];   // box 128 rows x 64 columns: A operand of the Gram phase
     const CUtensorMap* tm_xb[2];   // box (256 or 128) rows x 64 columns: B operand of the Gram phase
     const CUtensorMap* tm_xn[2];   // box 64 rows x (256 or 128) columns: B operand of the apply phase
-    const CUtensorMap* tm_gram;
-    const CUtensorMap* tm_poly;
+    const CUtensorMap* tm_gram;    // box 64 columns x 128 rows (A operand of the polynomial phase)
+    const CUtensorMap* tm_gram_b;  // box 64 columns x (256 or 128) rows (its B operand)
+    const CUtensorMap* tm_poly;    // box 64 columns x 128 rows (A operand of the apply phase)
     float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix),
                                // [2..4] = 1/lambda, 1/lambda^2, 1/sqrt(lambda) of the spectral
                                // estimate (1 under Frobenius scaling); kScaleStride floats

@@ -639,7 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         tma = md.tm_xa[step & 1];
                         tmb = md.tm_xb[step & 1];
                     } else if (ph == kPoly) {          // both from A (128-byte swizzle)
-                        tma = tmb = md.tm_gram;
+                        tma = md.tm_gram;
+                        tmb = md.tm_gram_b;
                     } else {                           // B (swizzled), then the blocked operand
                         tma = md.tm_poly;
                         tmb = md.tm_xn[step & 1];
@@ -679,15 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         });
                     } else if (ph == kPoly) {
                         k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
+                            // 128 rows of A and all B rows of the stage, one copy each
                             load2<kPair>(sa, tma, bar, k0, i0);
-                            load2<kPair>(sa + kBoxBytes, tma, bar, k0, i0 + kBox);
-#pragma unroll
-                            for (int q = 0; q < G::kBBoxes; ++q) load2<kPair>(sb + q * kBoxBytes, tmb, bar, k0, j0 + q * kBox);
+                            load2<kPair>(sb, tmb, bar, k0, j0);
                         });
                     } else {
                         k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
                             load2<kPair>(sa, tma, bar, k0, i0);
-                            load2<kPair>(sa + kBoxBytes, tma, bar, k0, i0 + kBox);
                             load3<kPair>(sb, tmb, bar, k0 >> 3, j0 >> 3);
                         });
                     }
