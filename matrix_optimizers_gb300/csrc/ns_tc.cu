@@ -608,8 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t armed[G::kStages];
-            for (int s = 0; s < G::kStages; ++s) armed[s] = 0;
+            uint32_t narmed = 0;                     // stages armed so far, in ring order
             bool ok = true;
             unsigned long long dep_wait_ns = 0, dep_spins = 0;
             for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
@@ -666,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                                 return;
                             }
                             if (leader) mbar_arrive_expect_tx(full, G::kTxBytes);
-                            ++armed[stage];
+                            ++narmed;
                             const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
                             const uint32_t bar = kPair ? mapa_shared(full, 0) : full;   // the leader's barrier
                             load(sa, sa + kABytes, bar, kk * kTcBK);
@@ -702,9 +701,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 // them all); in a pair the leader's barriers also count the
                 // peer's copies of the stages it armed
                 for (int s = 0; s < G::kStages; ++s) {
-                    if (armed[s] == 0) continue;
+                    // stage s was armed by the arms s, s + kStages, ...
+                    if (narmed <= static_cast<uint32_t>(s)) continue;
+                    const uint32_t times = (narmed - 1u - static_cast<uint32_t>(s)) / G::kStages + 1u;
                     const uint32_t full = smem_u32(&ctl->full[s]);
-                    const uint32_t par = (armed[s] - 1u) & 1u;
+                    const uint32_t par = (times - 1u) & 1u;
                     long long t0 = clock64();
                     while (!mbar_try_wait(full, par) && clock64() - t0 < kWaitCycles) {}
                 }
