@@ -14,11 +14,11 @@
 // A launch runs a range of (step, phase) levels.  With one level per launch
 // the kernel boundary orders the phases.  A fused launch runs all levels in
 // one cooperative persistent grid: each CTA walks its scheduled tiles level by
-// level, and a tile waits (producer, before its first TMA load) on per-matrix
+// level, and a tile waits (its loads, through the dependency warp) on per-matrix
 // completion counters that the epilogue warps release, so one matrix's next
 // phase starts as soon as its own inputs are complete.
 //
-// Roles per CTA (576 threads, one CTA per SM):
+// Roles per CTA (608 threads, one CTA per SM):
 //   warps 0-15 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
 //              global stores; warp w reads TMEM lanes 32*(w%4).. and the
 //              64-column slice w/4 of the 256-column accumulator (16 warps
@@ -28,7 +28,10 @@
 //   warp 17    TMEM allocator and single-thread tcgen05.mma issuer
 //              (M = 128, N = 256, K = 16 per instruction) into a double-
 //              buffered accumulator (2 x 256 TMEM columns), so the epilogue
-//              of one tile overlaps the main loop of the next.
+//              of one tile overlaps the main loop of the next;
+//   warp 18    dependency waits: runs ahead along the producer's tile list,
+//              acquires the completion counters a tile needs and hands the
+//              producer and epilogue a shared-memory count of cleared tiles.
 // Every barrier wait is bounded (see ptx.cuh); a timeout raises the CTA's
 // abort flag, records an error code and unwinds after draining copies.
 #include <cuda_bf16.h>
@@ -51,7 +54,8 @@ constexpr int kEpiWarps = kTcEpiWarps;                     // 4 lane quarters x 
 constexpr int kEpiSliceCols = kTcBN / (kEpiWarps / 4);     // 64 accumulator columns per epilogue warp
 constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr int kDepWarp = kEpiWarps + 2;
+constexpr int kThreads = 32 * (kEpiWarps + 3);
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStages = 6;
 
@@ -81,6 +85,8 @@ struct Ctl {
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
+    int dep_ready;             // tiles of this CTA's list whose inputs the dependency warp has acquired
+    int prod_seq;              // tiles of this CTA's list the producer has started loading
 };
 
 // ---------------------------------------------------------------- helpers
@@ -534,6 +540,48 @@ __device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, 
 // Gram tiles with at least this many K blocks alternate their K direction.
 constexpr int kReverseMinKBlocks = 64;
 
+// The producer's wait for the dependency warp to clear tile `seq` of the
+// CTA's list: a CTA-scope acquire of its count.  The dependency warp either
+// advances the count or raises the abort flag within its own bound, so this
+// wait's bound (that one plus the barrier bound) only guards against a bug.
+__device__ __forceinline__ bool wait_dep_ready(Ctl* ctl, int seq, volatile int* abort_flag, int* err,
+                                               long long limit) {
+    if (ld_acquire_cta_smem(&ctl->dep_ready) > seq) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(32);   // a tight spin would take issue slots from the epilogue warps beside it
+        if (ld_acquire_cta_smem(&ctl->dep_ready) > seq) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            atomicCAS(err, 0, 0x108);
+            return false;
+        }
+    }
+}
+
+// The dependency warp starts a tile's wait only once the producer has started
+// the tile this many places before it: early enough to take the acquire off
+// the producer's path, late enough that 152 CTAs do not poll a grid-wide
+// counter for a whole level (those polls crowd the L2 slice that serves it).
+constexpr int kDepLead = 2;
+
+__device__ __forceinline__ bool wait_producer_near(const Ctl* ctl, int seq, volatile int* abort_flag, int* err) {
+    const volatile int* ps = &ctl->prod_seq;
+    if (*ps + kDepLead >= seq) return true;
+    const long long t0 = clock64();
+    for (;;) {
+        __nanosleep(128);
+        if (*ps + kDepLead >= seq) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort_flag = 1;
+            atomicCAS(err, 0, 0x109);
+            return false;
+        }
+    }
+}
+
 // TMA loads of one box, the pair form counting on the leader's barrier.
 template <bool kPair>
 __device__ __forceinline__ void load2(uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int y) {
@@ -559,8 +607,8 @@ __device__ __forceinline__ int2 unit_tiles(const NsLaunch& p, int ph, int unit) 
 }  // namespace
 
 
-// 576 threads are 18 warps, so one of the SM's four sub-partitions holds 5
-// of them: its 16 K registers cap a thread at 96 (a larger per-kernel cap
+// 608 threads are 19 warps, so three of the SM's four sub-partitions hold 5
+// of them: 16 K registers per sub-partition cap a thread at 96 (a larger per-kernel cap
 // leaves the block unlaunchable).
 template <bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constant__ NsLaunch p) {
@@ -585,6 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
+        ctl->dep_ready = 0;
+        ctl->prod_seq = 0;
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -610,22 +660,24 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             uint32_t phase = 0;
             uint32_t narmed = 0;                     // stages armed so far, in ring order
             bool ok = true;
-            unsigned long long dep_wait_ns = 0, dep_spins = 0;
+            int seq = 0;                             // tiles so far in this CTA's list
             for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
                 const int ph = lv % 3, step = lv / 3;
                 const int2 range = unit_tiles(p, ph, unit);
-                const bool mn_b = ph == kApply;
                 int dep_key = -1;                    // counter set last seen met at this level
-                for (int t = 0; t < range.y && ok; ++t) {
+                for (int t = 0; t < range.y && ok; ++t, ++seq) {
                     const TileDesc td = p.tc_tiles[ph][range.x + t];
                     const MatDesc& md = p.mats[td.mat];
                     const int key = p.deps == 2 ? 0 : td.mat;
+                    if (p.deps) *static_cast<volatile int*>(&ctl->prod_seq) = seq;
                     if (p.deps && key != dep_key) {
-                        // (grid-wide counters serve every matrix: there every wait stalls)
-                        const bool stall = p.stall_mat >= 0 && (td.mat == p.stall_mat || p.deps == 2);
-                        const int w = wait_deps(p, deps_of(p, md), ph, step, stall, abort_flag, &dep_wait_ns);
-                        if (w == 0) { ok = false; break; }
-                        dep_spins += w == 2;
+                        // the dependency warp, running ahead along the same list, has
+                        // acquired the inputs of this tile and of the tiles after it
+                        // up to the next change of counter set
+                        if (!wait_dep_ready(ctl, seq, abort_flag, p.err, p.dep_wait_cycles + kWaitCycles)) {
+                            ok = false;
+                            break;
+                        }
                         fence_proxy_async_global();
                         dep_key = key;
                     }
@@ -690,10 +742,6 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         });
                     }
                 }
-            }
-            if (p.stamps != nullptr) {
-                p.stamps[4 * blockIdx.x + 2] = dep_wait_ns;
-                p.stamps[4 * blockIdx.x + 3] = dep_spins;
             }
             if (leader) {
                 // every armed copy lands before the CTA exits, also when the MMA
@@ -804,6 +852,43 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             long long t0 = clock64();
             while (!mbar_try_wait(smem_u32(&ctl->drain), 0) && clock64() - t0 < kWaitCycles) {}
         }
+    } else if (warp == kDepWarp) {
+        // Dependency warp: walks the CTA's tile list in the producer's order and,
+        // for each tile that starts a new matrix (per-matrix counters) or a new
+        // level (grid-wide counters), waits (bounded) until the tiles whose
+        // results it reads and whose inputs it overwrites have released their
+        // counters; then publishes the count of tiles so cleared.  Its gpu-scope
+        // acquires are off the producer's path, which reads the count with a
+        // CTA-scope acquire.
+        if (lane == 0 && p.deps) {
+            unsigned long long dep_wait_ns = 0, dep_spins = 0;
+            int seq = 0;
+            bool ok = true;
+            for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
+                const int ph = lv % 3, step = lv / 3;
+                const int2 range = unit_tiles(p, ph, unit);
+                int dep_key = -1;
+                for (int t = 0; t < range.y; ++t) {
+                    const TileDesc td = p.tc_tiles[ph][range.x + t];
+                    const int key = p.deps == 2 ? 0 : td.mat;
+                    if (key != dep_key) {
+                        if (!wait_producer_near(ctl, seq, abort_flag, p.err)) { ok = false; break; }
+                        // (grid-wide counters serve every matrix: there every wait stalls)
+                        const bool stall = p.stall_mat >= 0 && (td.mat == p.stall_mat || p.deps == 2);
+                        const int w = wait_deps(p, deps_of(p, p.mats[td.mat]), ph, step, stall, abort_flag,
+                                                &dep_wait_ns);
+                        if (w == 0) { ok = false; break; }
+                        dep_spins += w == 2;
+                        dep_key = key;
+                    }
+                    st_release_cta_smem(&ctl->dep_ready, ++seq);
+                }
+            }
+            if (p.stamps != nullptr) {
+                p.stamps[4 * blockIdx.x + 2] = dep_wait_ns;
+                p.stamps[4 * blockIdx.x + 3] = dep_spins;
+            }
+        }
     } else {
         const int quarter = warp & 3, slice = warp >> 2;
         const uint32_t tempty_leader[2] = {kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0) : 0u,
@@ -828,16 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 tc_fence_after();
                 if (p.deps && ph != kGram) {
                     // the Gram entries (poly), or the operand and B's diagonal
-                    // residual (apply), read below were released by other CTAs
-                    if (lane == 0) {
-                        const int* cnt = deps_of(p, md).cnt;
-                        if (ph == kPoly) {
-                            (void)ld_acquire_gpu(cnt + kGram);
-                        } else {
-                            (void)ld_acquire_gpu(cnt + kPoly);
-                            (void)ld_acquire_gpu(cnt + kApply);
-                        }
-                    }
+                    // residual (apply), read below were released by other CTAs and
+                    // acquired by the dependency warp before this tile was loaded
+                    if (lane == 0) (void)ld_acquire_cta_smem(&ctl->dep_ready);
                     __syncwarp();
                 }
                 const int i = td.ti * G::kTileRows + static_cast<int>(rank) * kTcBM + quarter * 32 + lane;
