@@ -197,7 +197,9 @@ def _sm_balance(st):
     if st.shape[2] >= 4 and st[:, :, 3].sum() > 0:
         busy_all = np.where(st[:, :, 1] > 0, st[:, :, 1] - st[:, :, 0], 0).astype(np.float64)
         waits = {"dep_wait_frac_of_busy": float(st[:, :, 2].sum() / max(1.0, busy_all.sum())),
-                 "dep_spinning_waits_per_cta_launch": float(st[:, :, 3].mean())}
+                 "dep_spinning_waits_per_cta_launch": float(st[:, :, 3].mean()),
+                 "dep_wait_what": "time the dependency warp spent waiting on completion counters; it runs up to "
+                                  "two tiles ahead of the producer, so most of it overlaps loads and MMAs"}
     return {"launches": len(ratios), "ctas_per_launch_max": int(st.shape[1]), **waits,
             "max_over_mean_busy": sum_max / sum_mean,
             "per_launch_median": float(np.median(ratios)), "per_launch_worst": float(np.max(ratios)),
