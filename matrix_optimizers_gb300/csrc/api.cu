@@ -82,6 +82,19 @@ bool encode_bf16_map(CUtensorMap* map, const void* base, int64_t rows, int64_t c
     return r == CUDA_SUCCESS;
 }
 
+// Store view of an m x m bf16 buffer for the symmetric epilogues: 32 x 32
+// boxes (64-byte rows) with the 64-byte swizzle their shared-memory staging uses.
+bool encode_bf16_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Descriptor strides of the apply phase's MN-major B operand (no swizzle:
 // 8-row K groups 128 B apart, 8-column MN blocks 1 KB apart), as (lbo, sbo).
 constexpr uint32_t kMnLbo = 128, kMnSbo = 1024;
@@ -155,7 +168,7 @@ Shape oriented(int64_t rows, int64_t cols) {
 // (8 rows x 8 columns of one block, 128 contiguous bytes), row groups of 8,
 // column blocks.  A box of `rows` x `cols` of X lands in shared memory as
 // [column block][row][8 elements], the no-swizzle canonical layout.
-constexpr int kMapsPerMatrix = 9;    // 3 views of each operand buffer, 2 of the Gram matrix, polynomial
+constexpr int kMapsPerMatrix = 11;   // 3 views of each operand buffer, 2 of the Gram matrix, polynomial, 2 store views
 bool encode_xop_map(CUtensorMap* map, const void* base, const Shape& s, int rows, int cols) {
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(s.xrows / 8), static_cast<cuuint64_t>(s.xblocks)};
     cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(s.xrows * 16)};
@@ -493,12 +506,16 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
             if (!encode_bf16_map(&hm0[6], d.gram, s.m, s.m, s.lda, kTcBM)) return MO_ERR_CUDA;
             if (!encode_bf16_map(&hm0[7], d.gram, s.m, s.m, s.lda, bn)) return MO_ERR_CUDA;
             if (!encode_bf16_map(&hm0[8], d.poly, s.m, s.m, s.lda, kTcBM)) return MO_ERR_CUDA;
+            if (!encode_bf16_store_map(&hm0[9], d.gram, s.m, s.m, s.lda)) return MO_ERR_CUDA;
+            if (!encode_bf16_store_map(&hm0[10], d.poly, s.m, s.m, s.lda)) return MO_ERR_CUDA;
             d.tm_gram = dm0 + 6;
             d.tm_gram_b = dm0 + 7;
             d.tm_poly = dm0 + 8;
+            d.tm_gram_st = dm0 + 9;
+            d.tm_poly_st = dm0 + 10;
         } else {
             for (int q = 0; q < 2; ++q) d.tm_xa[q] = d.tm_xb[q] = d.tm_xn[q] = nullptr;
-            d.tm_gram = d.tm_gram_b = d.tm_poly = nullptr;
+            d.tm_gram = d.tm_gram_b = d.tm_poly = d.tm_gram_st = d.tm_poly_st = nullptr;
         }
     }
 

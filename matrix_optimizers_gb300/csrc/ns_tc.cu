@@ -20,7 +20,8 @@
 //
 // Roles per CTA (608 threads, one CTA per SM):
 //   warps 0-15 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
-//              global stores; warp w reads TMEM lanes 32*(w%4).. and the
+//              stores (the symmetric phases' through a 2 KB shared-memory
+//              block per warp and TMA); warp w reads TMEM lanes 32*(w%4).. and the
 //              64-column slice w/4 of the 256-column accumulator (16 warps
 //              keep the memory-heavy apply epilogue shorter than a main loop);
 //   warp 16    TMA producer: 64 x 64 bf16 boxes (128-byte swizzle) into a
@@ -58,6 +59,7 @@ constexpr int kDepWarp = kEpiWarps + 2;
 constexpr int kThreads = 32 * (kEpiWarps + 3);
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxStages = 6;
+constexpr int kEpiStageBytes = 32 * 32 * 2;                // one epilogue warp's 32 x 32 bf16 store block
 
 // Tile geometry.  Single CTA (cta_group::1): a 128 x 256 tile per CTA, the
 // stage holding 128 rows of A and all 256 columns of B.  CTA pair
@@ -70,14 +72,15 @@ struct Geo {
     static constexpr int kBBoxes = kPair ? 2 : 4;            // 64-wide B boxes per CTA and stage
     static constexpr int kStageBytes = kABytes + kBBoxes * kBoxBytes;
     static constexpr int kTileRows = kPair ? 2 * kTcBM : kTcBM;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 1024;
+    // ring, control block (1 KB), the epilogue warps' store staging, alignment slack
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kEpiWarps * kEpiStageBytes + 1024;
     static constexpr int kTxBytes = (kPair ? 2 : 1) * kStageBytes;   // counted on the leader's full barrier
     static constexpr uint32_t kTemptyCount = (kPair ? 2 : 1) * kEpiWarps;
 };
 static_assert(Geo<true>::kStages <= kMaxStages && Geo<false>::kStages <= kMaxStages, "ring depth");
 static_assert(Geo<true>::kSmemBytes <= 232448 && Geo<false>::kSmemBytes <= 232448, "shared memory");
 
-struct Ctl {
+struct Ctl {                   // 1 KB after the ring; the store staging follows
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t tfull[2];
@@ -88,6 +91,7 @@ struct Ctl {
     int dep_ready;             // tiles of this CTA's list whose inputs the dependency warp has acquired
     int prod_seq;              // tiles of this CTA's list the producer has started loading
 };
+static_assert(sizeof(Ctl) <= 1024, "control block");
 
 // ---------------------------------------------------------------- helpers
 __device__ __forceinline__ void unpack_bf16x8(const uint4& u, float* v) {
@@ -297,18 +301,42 @@ __device__ __forceinline__ void user_store32(const MatDesc& md, void* p, int dt,
 }
 
 // ------------------------------------------------------------- epilogues
-// Symmetric phases: keep elements with j >= i, store at (i, j) and (j, i).
-__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int phase, int step, int i,
-                                              int j0, float (&v)[32]) {
+// Symmetric phases.  The warp holds the 32 x 32 block of rows i0 + lane
+// and columns j0 .. j0 + 31 (one row per lane).  Blocks below the diagonal
+// are dropped; a block above it is stored at (i0, j0) and, transposed, at
+// (j0, i0); a diagonal block (j0 == i0) is stored once, holding the upper
+// values in both triangles, so each element of the symmetric result comes
+// from the one upper-triangle accumulator entry.  The blocks go out through
+// the warp's 2 KB shared-memory block and TMA stores (a warp's scattered
+// 32- and 64-byte row pieces measured several times slower).  The staging
+// uses the 64-byte swizzle of the store view: 16-byte chunk c of row r sits
+// at chunk c ^ ((r >> 1) & 3), which spreads a warp's writes over all banks.
+__device__ __forceinline__ uint32_t stage_off(int r, int c16) {
+    return static_cast<uint32_t>(r * 64 + ((c16 ^ ((r >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t a, const uint4& v) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_b16(uint32_t a, bf16 v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<unsigned short*>(&v)) : "memory");
+}
+
+// Called by all 32 lanes of the warp; lane 0 issues the stores.  `sbuf` is
+// the warp's staging block (shared-memory address).
+__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int phase, int step, int i0,
+                                              int j0, float (&v)[32], uint32_t sbuf) {
+    const int lane = threadIdx.x & 31;
     const int m = md.m;
-    if (j0 + 31 < i || j0 >= m) return;
-    bf16* dst = static_cast<bf16*>(phase == kGram ? md.gram : md.poly);
+    if (j0 < i0 || j0 >= m || i0 >= m) return;                  // warp-uniform
+    const int i = i0 + lane;
+    const bool row_ok = i < m;
     const int nv = min(32, m - j0);
     if (phase == kGram) {
         const float sc = step == 0 ? md.scales[1] : 1.f;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] *= sc;
-    } else {
+    } else if (row_ok) {
         float a[32];
         load32_bf16_l2(static_cast<const bf16*>(md.gram), static_cast<int64_t>(i) * md.lda + j0, nv, a);
         // step 0 folds the spectral scale into the coefficients (1 otherwise);
@@ -328,18 +356,43 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
             md.dlo[i] = dv - __bfloat162float(__float2bfloat16_rn(dv));
         }
     }
-    const int64_t row = static_cast<int64_t>(i) * md.lda;
-    if (j0 >= i) {
-        store32(dst, MO_BF16, row + j0, nv, v);
-    } else {
+    const CUtensorMap* tm = phase == kGram ? md.tm_gram_st : md.tm_poly_st;
+    if (lane == 0) bulk_wait_read_all();             // the last store has read the block
+    __syncwarp();
+    if (j0 != i0) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) st_shared_v4(sbuf + stage_off(lane, c), pack_bf16x8(&v[8 * c]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, sbuf, j0, i0);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+        __syncwarp();
+        // the transpose: row k of the block at (j0, i0) is column k of this one
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-            if (j0 + k >= i && k < nv) dst[row + j0 + k] = __float2bfloat16_rn(v[k]);
-    }
+            st_shared_b16(sbuf + stage_off(k, lane >> 3) + (lane & 7) * 2, __float2bfloat16_rn(v[k]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, sbuf, i0, j0);
+            bulk_commit();
+        }
+    } else {
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        const int j = j0 + k;
-        if (j > i && k < nv) dst[static_cast<int64_t>(j) * md.lda + i] = __float2bfloat16_rn(v[k]);
+        for (int k = 0; k < 32; ++k) {
+            const bf16 h = __float2bfloat16_rn(v[k]);
+            if (k >= lane) st_shared_b16(sbuf + stage_off(lane, k >> 3) + (k & 7) * 2, h);
+            if (k > lane) st_shared_b16(sbuf + stage_off(k, lane >> 3) + (lane & 7) * 2, h);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tm, sbuf, j0, i0);
+            bulk_commit();
+        }
     }
 }
 
@@ -935,8 +988,9 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
                     if (ph == kApply)
                         epi_apply(p, md, step, i, row_ok, j0, v);
-                    else if (row_ok)
-                        epi_symmetric(p, md, ph, step, i, j0, v);
+                    else
+                        epi_symmetric(p, md, ph, step, i - lane, j0, v,
+                                      smem_u32(smem + G::kStages * G::kStageBytes + 1024 + warp * kEpiStageBytes));
                 }
                 // the accumulator is in registers by now: hand it back to the
                 // MMA warp before waiting for this tile's stores to drain
@@ -949,12 +1003,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         mbar_arrive_cluster(tempty_leader[acc]);
                 }
                 if (p.deps) {
+                    if (lane == 0 && ph != kApply) bulk_wait_all();   // the tile's TMA stores have landed
                     fence_proxy_async_global();   // the stores above feed later TMA loads
                     __syncwarp();
                     if (lane == 0) red_release_gpu_add(deps_of(p, md).cnt + ph, 1);
                 }
             }
         }
+        if (lane == 0) bulk_wait_all();           // no store still reads this CTA's shared memory
     }
 
     __syncwarp();
