@@ -95,6 +95,22 @@ bool encode_bf16_store_map(CUtensorMap* map, const void* base, int64_t rows, int
     return r == CUDA_SUCCESS;
 }
 
+// The user's W for the last step's update: boxes of 32 rows x 64 bytes (16
+// fp32 or 32 bf16 columns), 64-byte swizzle.  False when W's address or row
+// pitch is not 16-byte aligned (TMA's rule); the update then uses plain accesses.
+bool encode_w_map(CUtensorMap* map, const void* W, int dtype, int64_t rows, int64_t cols, int64_t ld) {
+    const int64_t esz = dtype == MO_F32 ? 4 : 2;
+    if ((reinterpret_cast<uintptr_t>(W) & 15) != 0 || (ld * esz) % 16 != 0) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * esz)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / esz), 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, dtype == MO_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                          const_cast<void*>(W), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Descriptor strides of the apply phase's MN-major B operand (no swizzle:
 // 8-row K groups 128 B apart, 8-column MN blocks 1 KB apart), as (lbo, sbo).
 constexpr uint32_t kMnLbo = 128, kMnSbo = 1024;
@@ -168,7 +184,7 @@ Shape oriented(int64_t rows, int64_t cols) {
 // (8 rows x 8 columns of one block, 128 contiguous bytes), row groups of 8,
 // column blocks.  A box of `rows` x `cols` of X lands in shared memory as
 // [column block][row][8 elements], the no-swizzle canonical layout.
-constexpr int kMapsPerMatrix = 11;   // 3 views of each operand buffer, 2 of the Gram matrix, polynomial, 2 store views
+constexpr int kMapsPerMatrix = 12;   // 3 views of each operand buffer, 2 of the Gram matrix, polynomial, 2 store views, W
 bool encode_xop_map(CUtensorMap* map, const void* base, const Shape& s, int rows, int cols) {
     cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(s.xrows / 8), static_cast<cuuint64_t>(s.xblocks)};
     cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(s.xrows * 16)};
@@ -513,9 +529,10 @@ int build_plan(const std::vector<Job>& jobs, int precision, void* ws, bool pair,
             d.tm_poly = dm0 + 8;
             d.tm_gram_st = dm0 + 9;
             d.tm_poly_st = dm0 + 10;
+            d.tm_w = j.W != nullptr && encode_w_map(&hm0[11], j.W, j.w_dtype, j.rows, j.cols, j.ld) ? dm0 + 11 : nullptr;
         } else {
             for (int q = 0; q < 2; ++q) d.tm_xa[q] = d.tm_xb[q] = d.tm_xn[q] = nullptr;
-            d.tm_gram = d.tm_gram_b = d.tm_poly = d.tm_gram_st = d.tm_poly_st = nullptr;
+            d.tm_gram = d.tm_gram_b = d.tm_poly = d.tm_gram_st = d.tm_poly_st = d.tm_w = nullptr;
         }
     }
 

@@ -71,6 +71,8 @@ struct MatDesc {
     const CUtensorMap* tm_poly;    // box 64 columns x 128 rows (A operand of the apply phase)
     const CUtensorMap* tm_gram_st; // box 32 x 32, 64-byte swizzle: the Gram epilogue's stores of A
     const CUtensorMap* tm_poly_st; // box 32 x 32, 64-byte swizzle: the polynomial epilogue's stores of B
+    const CUtensorMap* tm_w;       // user W, 64-byte rows x 32 rows, 64-byte swizzle: the last step's
+                                   // update (null: W unaligned for TMA, updated by plain accesses)
     float* scales;             // [0] = 1/||X||_F, [1] = 1/||X||_F^2 (0 for a zero matrix),
                                // [2..4] = 1/lambda, 1/lambda^2, 1/sqrt(lambda) of the spectral
                                // estimate (1 under Frobenius scaling); kScaleStride floats

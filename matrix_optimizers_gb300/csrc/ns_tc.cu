@@ -86,6 +86,7 @@ struct Ctl {                   // 1 KB after the ring; the store staging follows
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t wbar[kEpiWarps];  // per epilogue warp: its W box has landed in its staging block
     uint32_t tmem_base;
     int abort_flag;
     int dep_ready;             // tiles of this CTA's list whose inputs the dependency warp has acquired
@@ -447,12 +448,104 @@ __device__ __forceinline__ void load_diag_fix(const MatDesc& md, int step, int i
         if (j0 + 8 * q < md.n) xr[q] = __ldcg(src + static_cast<int64_t>(q) * md.xrows);
 }
 
+// Last-step weight update W <- W - decay W - alpha X' of the warp's 32 x 32
+// block through its staging block: a TMA load of W's box (32 rows x 64 B:
+// 16 fp32 or 32 bf16 columns, so an fp32 block takes two), the update in
+// shared memory, a TMA store back.  Each lane's own 32-byte row pieces of W,
+// 32 rows per warp instruction, measured about three times slower.  In the
+// transposed frame the box's rows are W's rows j0 .. j0 + 31 and a lane
+// reads a column of it.  `wuse` counts the warp's W boxes (the parity of its
+// barrier); `wpend` is set while a box may still be landing (a wait that
+// gave up), for the drain before the CTA exits.  Called by all 32 lanes.
+__device__ __forceinline__ bool epi_update_tma(const NsLaunch& p, const MatDesc& md, int i0, int j0,
+                                               const float (&x)[32], uint32_t sbuf, uint32_t wbar, uint32_t& wuse,
+                                               bool& wpend, volatile int* abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const bool f32 = md.w_dtype == MO_F32;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        if (h == 1 && !f32) break;
+        const int off = f32 ? 16 * h : 0;
+        const int bx = md.transposed ? i0 + off : j0 + off;
+        const int by = md.transposed ? j0 : i0;
+        if (lane == 0) {
+            bulk_wait_read_all();                    // the last store has read the block
+            mbar_arrive_expect_tx(wbar, kEpiStageBytes);
+            tma_load_2d(sbuf, md.tm_w, wbar, bx, by);
+        }
+        wpend = true;
+        const bool ok = mbar_wait_bounded(wbar, wuse & 1u, abort_flag, p.err, 0x106);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        wpend = false;
+        ++wuse;
+        if (!md.transposed) {
+            // lane = row: 4 chunks of 16 bytes
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t a = sbuf + stage_off(lane, c);
+                uint4 u;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                             : "r"(a)
+                             : "memory");
+                if (f32) {
+                    float w[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                  __uint_as_float(u.w)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) w[e] = fmaf(-p.alpha, x[off + 4 * c + e], w[e] - p.decay * w[e]);
+                    u = make_uint4(__float_as_uint(w[0]), __float_as_uint(w[1]), __float_as_uint(w[2]),
+                                   __float_as_uint(w[3]));
+                } else {
+                    float w[8];
+                    unpack_bf16x8(u, w);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) w[e] = fmaf(-p.alpha, x[8 * c + e], w[e] - p.decay * w[e]);
+                    u = pack_bf16x8(w);
+                }
+                st_shared_v4(a, u);
+            }
+        } else if (f32) {
+            // lanes 16h .. 16h + 15 own the box's columns (their rows of X')
+            if ((lane >> 4) == h) {
+                const int col = lane & 15;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const uint32_t a = sbuf + stage_off(k, col >> 2) + (col & 3) * 4;
+                    float w;
+                    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(w) : "r"(a) : "memory");
+                    w = fmaf(-p.alpha, x[k], w - p.decay * w);
+                    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(w) : "memory");
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const uint32_t a = sbuf + stage_off(k, lane >> 3) + (lane & 7) * 2;
+                unsigned short hb;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hb) : "r"(a) : "memory");
+                float w = __uint_as_float(static_cast<uint32_t>(hb) << 16);
+                w = fmaf(-p.alpha, x[k], w - p.decay * w);
+                st_shared_b16(a, __float2bfloat16_rn(w));
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(md.tm_w, sbuf, bx, by);
+            bulk_commit();
+        }
+    }
+    return true;
+}
+
 // Called by all 32 lanes of a warp (the fused pack takes warp ballots);
 // lanes whose row lies beyond the matrix touch no memory.
-__device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, int step, int i, bool row_ok,
-                                          int j0, float (&v)[32]) {
+// Returns false when a wait of the weight update gave up.
+__device__ __forceinline__ bool epi_apply(const NsLaunch& p, const MatDesc& md, int step, int i, bool row_ok,
+                                          int j0, float (&v)[32], uint32_t sbuf, uint32_t wbar, uint32_t& wuse,
+                                          bool& wpend, volatile int* abort_flag) {
     const int n = md.n;
-    if (j0 >= n) return;
+    if (j0 >= n) return true;
     const int nv = row_ok ? min(32, n - j0) : 0;
     uint4 xr[4];
     float di;
@@ -472,20 +565,22 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     if (step + 1 < p.steps) {
         // the next operand, in 8-column blocks: the warp's 32 rows of one block
         // are 512 contiguous bytes (columns past n hold the accumulator's zeros)
-        if (!row_ok) return;
+        if (!row_ok) return true;
         uint4* dst = static_cast<uint4*>(md.x_op[(step + 1) & 1]) + static_cast<int64_t>(j0 >> 3) * md.xrows + i;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
             if (j0 + 8 * q < n) dst[static_cast<int64_t>(q) * md.xrows] = pack_bf16x8(&x[8 * q]);
-        return;
+        return true;
     }
     if (md.sign_words != nullptr) {
         epi_sign_pack(md, i, row_ok, j0, min(32, n - j0), x);
-        return;
+        return true;
     }
-    if (!row_ok) return;
+    if (p.apply_update && md.W != nullptr && md.tm_w != nullptr)
+        return epi_update_tma(p, md, i - (threadIdx.x & 31), j0, x, sbuf, wbar, wuse, wpend, abort_flag);
+    if (!row_ok) return true;
     if (p.apply_update) {
-        if (md.W == nullptr) return;
+        if (md.W == nullptr) return true;
         float w[32];
         user_load32(md, md.W, md.w_dtype, i, j0, nv, w);
 #pragma unroll
@@ -494,6 +589,7 @@ __device__ __forceinline__ void epi_apply(const NsLaunch& p, const MatDesc& md, 
     } else if (md.out != nullptr) {
         user_store32(md, md.out, md.out_dtype, i, j0, nv, x);
     }
+    return true;
 }
 
 // Last NS step with the weight update: while the epilogue waits for the
@@ -685,6 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             mbar_init(smem_u32(&ctl->tempty[a]), G::kTemptyCount);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
+        for (int w = 0; w < kEpiWarps; ++w) mbar_init(smem_u32(&ctl->wbar[w]), 1);
         ctl->abort_flag = 0;
         ctl->dep_ready = 0;
         ctl->prod_seq = 0;
@@ -948,6 +1045,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                                            kPair ? mapa_shared(smem_u32(&ctl->tempty[1]), 0) : 0u};
         bool ok = true;
         int q = 0;
+        uint32_t wuse = 0;                        // W boxes this warp has loaded (its barrier's parity)
+        bool wpend = false;                       // a W box may still be landing after a wait gave up
         for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
             const int ph = lv % 3, step = lv / 3;
             const int2 range = unit_tiles(p, ph, unit);
@@ -986,9 +1085,14 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     float v[32];
 #pragma unroll
                     for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
-                    if (ph == kApply)
-                        epi_apply(p, md, step, i, row_ok, j0, v);
-                    else
+                    if (ph == kApply) {
+                        if (!epi_apply(p, md, step, i, row_ok, j0, v,
+                                       smem_u32(smem + G::kStages * G::kStageBytes + 1024 + warp * kEpiStageBytes),
+                                       smem_u32(&ctl->wbar[warp]), wuse, wpend, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                    } else
                         epi_symmetric(p, md, ph, step, i - lane, j0, v,
                                       smem_u32(smem + G::kStages * G::kStageBytes + 1024 + warp * kEpiStageBytes));
                 }
@@ -1010,7 +1114,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                 }
             }
         }
-        if (lane == 0) bulk_wait_all();           // no store still reads this CTA's shared memory
+        if (lane == 0) {
+            bulk_wait_all();                      // no store still reads this CTA's shared memory
+            if (wpend) {                          // nor does a W box land in it after the CTA left
+                const long long t0 = clock64();
+                while (!mbar_try_wait(smem_u32(&ctl->wbar[warp]), wuse & 1u) && clock64() - t0 < kWaitCycles) {}
+            }
+        }
     }
 
     __syncwarp();
