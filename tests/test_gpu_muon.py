@@ -125,6 +125,45 @@ def test_bf16_state_dtypes():
     assert rel_fro(to_np(M), Mn) < 4e-3
 
 
+@pytest.mark.parametrize("rows,cols,ld,wdt", [
+    (100, 264, 268, "f32"),     # ragged 32-row boxes, padded rows
+    (264, 100, 104, "f32"),     # transposed frame
+    (96, 320, 328, "bf16"),
+    (320, 96, 104, "bf16"),
+])
+def test_update_through_w_boxes(rows, cols, ld, wdt):
+    """The last-step update loads and stores W in 32-row boxes: partial boxes at
+    the matrix edge, padded rows and the transposed frame give the oracle's
+    update, and the padding columns keep their values."""
+    rng = np.random.default_rng(rows + 3 * cols)
+    W0 = (0.02 * rng.standard_normal((rows, cols))).astype(np.float32) if wdt == "f32" else \
+        np.zeros((rows, cols), dtype=np.float32)       # bf16 W: see test_bf16_state_dtypes
+    G0 = rng.standard_normal((rows, cols)).astype(np.float32)
+    wt = torch.float32 if wdt == "f32" else torch.bfloat16
+    sentinel = 7.0
+
+    def padded(a, dtype):
+        big = torch.full((rows, ld), sentinel, dtype=dtype, device=dev())
+        big[:, :cols] = to_dev(a, dtype)
+        return big, big[:, :cols]
+
+    Wb, W = padded(W0, wt)
+    Mb, M = padded(np.zeros_like(G0), torch.float32)
+    Gb, G = padded(G0, torch.float32)
+    W0q = to_np(W)
+    mats = [mo.make_matrix(W, M, G)]
+    cfg = mo.make_cfg(mu=0.95, lr=0.05)
+    ws = workspace(mo.mo_workspace_bytes(mats, cfg))
+    mo.muon_step_batched(mats, cfg, ws)
+    torch.cuda.synchronize()
+    assert mo.mo_check_device_status(ws) == 0
+    Wn, _, _ = om.muon_step(W0q.astype(np.float64), np.zeros_like(W0q, dtype=np.float64), G0.astype(np.float64),
+                            mu=0.95, lr=0.05)
+    tol = NS_BF16_TOL if wdt == "f32" else 3e-2
+    assert rel_fro(to_np(W) - W0q, Wn - W0q) < tol
+    assert bool((Wb[:, cols:] == sentinel).all())
+
+
 def test_apply_update_off_writes_output():
     rng = np.random.default_rng(11)
     shapes = [(256, 384), (384, 256)]
