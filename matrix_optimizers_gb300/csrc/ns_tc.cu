@@ -323,13 +323,18 @@ __device__ __forceinline__ void st_shared_b16(uint32_t a, bf16 v) {
     asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(*reinterpret_cast<unsigned short*>(&v)) : "memory");
 }
 
-// Called by all 32 lanes of the warp; lane 0 issues the stores.  `sbuf` is
-// the warp's staging block (shared-memory address).
-__device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& md, int phase, int step, int i0,
-                                              int j0, float (&v)[32], uint32_t sbuf) {
+// Called by all 32 lanes of the warp; lane 0 issues the copies.  `sbuf` is
+// the warp's staging block (shared-memory address), `wbar` its barrier and
+// `wuse` / `wpend` its use count and in-flight flag (see epi_update_tma).
+// The polynomial phase's A block, read for bA, comes into the staging block by
+// a TMA load (each lane's 32-byte pieces, 32 rows per instruction, are many
+// small requests).  Returns false when that wait gave up.
+__device__ __forceinline__ bool epi_symmetric(const NsLaunch& p, const MatDesc& md, int phase, int step, int i0,
+                                              int j0, float (&v)[32], uint32_t sbuf, uint32_t wbar, uint32_t& wuse,
+                                              bool& wpend, volatile int* abort_flag) {
     const int lane = threadIdx.x & 31;
     const int m = md.m;
-    if (j0 < i0 || j0 >= m || i0 >= m) return;                  // warp-uniform
+    if (j0 < i0 || j0 >= m || i0 >= m) return true;             // warp-uniform
     const int i = i0 + lane;
     const bool row_ok = i < m;
     const int nv = min(32, m - j0);
@@ -337,9 +342,28 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
         const float sc = step == 0 ? md.scales[1] : 1.f;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] *= sc;
-    } else if (row_ok) {
+    } else {
+        if (lane == 0) {
+            bulk_wait_read_all();                    // the last store has read the block
+            if (p.deps) fence_proxy_async_global();  // A was released by other CTAs
+            mbar_arrive_expect_tx(wbar, kEpiStageBytes);
+            tma_load_2d(sbuf, md.tm_gram_st, wbar, j0, i0);
+        }
+        wpend = true;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(wbar, wuse & 1u, abort_flag, p.err, 0x107))) return false;
+        wpend = false;
+        ++wuse;
         float a[32];
-        load32_bf16_l2(static_cast<const bf16*>(md.gram), static_cast<int64_t>(i) * md.lda + j0, nv, a);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint4 u;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                         : "r"(sbuf + stage_off(lane, c))
+                         : "memory");
+            unpack_bf16x8(u, &a[8 * c]);
+        }
+        __syncwarp();                                // the block is read: the stores may reuse it
         // step 0 folds the spectral scale into the coefficients (1 otherwise);
         // the diagonal also takes a: B = bA + cA^2 + aI, so that the apply
         // phase is the plain product X' = B X
@@ -347,7 +371,7 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
         const float cs = step == 0 ? p.c * md.scales[3] : p.c;
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = fmaf(cs, v[k], bs * a[k]) + (j0 + k == i ? p.a : 0.f);
-        if (i >= j0 && i < j0 + nv) {
+        if (row_ok && i >= j0 && i < j0 + nv) {
             // the diagonal lies near a = 3.44, where the bf16 spacing is 2^-6:
             // keep its rounding residual (exact in fp32) for the apply epilogue
             float dv = 0.f;
@@ -395,6 +419,7 @@ __device__ __forceinline__ void epi_symmetric(const NsLaunch& p, const MatDesc& 
             bulk_commit();
         }
     }
+    return true;
 }
 
 // Fused Sign-Muon sign + 1-bit pack of the last step's output: bit = 1
@@ -1092,9 +1117,12 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                             ok = false;
                             break;
                         }
-                    } else
-                        epi_symmetric(p, md, ph, step, i - lane, j0, v,
-                                      smem_u32(smem + G::kStages * G::kStageBytes + 1024 + warp * kEpiStageBytes));
+                    } else if (!epi_symmetric(p, md, ph, step, i - lane, j0, v,
+                                              smem_u32(smem + G::kStages * G::kStageBytes + 1024 + warp * kEpiStageBytes),
+                                              smem_u32(&ctl->wbar[warp]), wuse, wpend, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                 }
                 // the accumulator is in registers by now: hand it back to the
                 // MMA warp before waiting for this tile's stores to drain
