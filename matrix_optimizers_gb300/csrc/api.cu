@@ -701,7 +701,7 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     np.level_deps = reinterpret_cast<int*>(base + L.deps) + 4 * jobs.size();
     np.tot_sym = static_cast<int32_t>(plan->ntiles[kGram]);
     np.tot_apply = static_cast<int32_t>(plan->ntiles[kApply]);
-    np.rel_per_tile = kTcEpiWarps * cta_per_unit;
+    np.rel_per_tile = kTcEpiGroupWarps * cta_per_unit;
     const uint32_t mma_m = static_cast<uint32_t>(kTcBM * cta_per_unit);
     np.idesc_sym = idesc_bf16_f32(mma_m, kTcBN, 0u);
     np.idesc_apply = idesc_bf16_f32(mma_m, kTcBN, 1u);
@@ -1249,7 +1249,7 @@ int mo_debug_ns_view(const int64_t* rows, const int64_t* cols, int n, int precis
     const bool pair = precision == MO_NS_BF16 && g_ns_pair.load() != 0 && tc_capacity(true) >= 2;
     view->tiles_sym = static_cast<int32_t>(sym_tiles(s.m, pair));
     view->tiles_apply = static_cast<int32_t>(apply_tiles(s.m, s.n, pair));
-    view->releases_per_tile = kTcEpiWarps * (pair ? 2 : 1);
+    view->releases_per_tile = kTcEpiGroupWarps * (pair ? 2 : 1);
     view->reserved = 0;
     return MO_OK;
 }

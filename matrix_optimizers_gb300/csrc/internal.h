@@ -15,6 +15,7 @@ constexpr int kTcBM = 128;   // rows of D per tile (TMEM lanes)
 constexpr int kTcBN = 256;   // columns of D per tile (TMEM columns per accumulator)
 constexpr int kTcBK = 64;    // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int kTcEpiWarps = 16;   // epilogue warps per CTA of the tensor-core kernel
+constexpr int kTcEpiGroupWarps = 8;   // of which one group finishes a tile (the groups alternate tiles)
 // Tile geometry of the CUDA-core fp32 GEMM.
 constexpr int kFpBM = 64, kFpBN = 64, kFpBK = 16;
 // Momentum / normalisation kernel tile.
@@ -115,7 +116,7 @@ struct NsLaunch {
                                // counter set (every tile of a level waits for the whole previous level)
     int* level_deps;           // [3] the grid-wide counters of mode 2
     int32_t tot_sym, tot_apply;  // tiles of one symmetric / apply level over all matrices
-    int32_t rel_per_tile;      // counter releases per finished tile (16 epilogue warps per CTA)
+    int32_t rel_per_tile;      // counter releases per finished tile (one group of 8 epilogue warps per CTA)
     uint32_t idesc_sym, idesc_apply;
     uint32_t mn_lbo, mn_sbo;   // descriptor strides of the MN-major operand
     unsigned long long* stamps;  // null, or [4 * gridDim.x]: per CTA start / end %globaltimer (ns),

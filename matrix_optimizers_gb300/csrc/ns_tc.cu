@@ -21,9 +21,10 @@
 // Roles per CTA (608 threads, one CTA per SM):
 //   warps 0-15 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
 //              stores (the symmetric phases' through a 2 KB shared-memory
-//              block per warp and TMA); warp w reads TMEM lanes 32*(w%4).. and the
-//              64-column slice w/4 of the 256-column accumulator (16 warps
-//              keep the memory-heavy apply epilogue shorter than a main loop);
+//              block per warp and TMA); two groups of 8 warps take alternate
+//              tiles (accumulator 0 and 1), so one group's stores drain while
+//              the other works; warp w reads TMEM lanes 32*(w%4).. and the
+//              128-column slice (w/4)%2 of its group's accumulator;
 //   warp 16    TMA producer: 64 x 64 bf16 boxes (128-byte swizzle) into a
 //              4-stage shared-memory ring (48 KB per stage);
 //   warp 17    TMEM allocator and single-thread tcgen05.mma issuer
@@ -51,8 +52,9 @@ namespace {
 constexpr int kBox = 64;                                   // TMA box edge (elements)
 constexpr int kBoxBytes = kBox * kBox * 2;                 // 8 KB
 constexpr int kABytes = kTcBM * kTcBK * 2;                 // 16 KB: 128 rows of A per CTA
-constexpr int kEpiWarps = kTcEpiWarps;                     // 4 lane quarters x 4 column slices
-constexpr int kEpiSliceCols = kTcBN / (kEpiWarps / 4);     // 64 accumulator columns per epilogue warp
+constexpr int kEpiWarps = kTcEpiWarps;                     // two groups of 8 that alternate tiles
+constexpr int kEpiGroupWarps = kTcEpiGroupWarps;           // 4 lane quarters x 2 column slices
+constexpr int kEpiSliceCols = kTcBN / (kEpiGroupWarps / 4);  // 128 accumulator columns per epilogue warp
 constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
 constexpr int kDepWarp = kEpiWarps + 2;
@@ -75,7 +77,7 @@ struct Geo {
     // ring, control block (1 KB), the epilogue warps' store staging, alignment slack
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kEpiWarps * kEpiStageBytes + 1024;
     static constexpr int kTxBytes = (kPair ? 2 : 1) * kStageBytes;   // counted on the leader's full barrier
-    static constexpr uint32_t kTemptyCount = (kPair ? 2 : 1) * kEpiWarps;
+    static constexpr uint32_t kTemptyCount = (kPair ? 2 : 1) * kEpiGroupWarps;
 };
 static_assert(Geo<true>::kStages <= kMaxStages && Geo<false>::kStages <= kMaxStages, "ring depth");
 static_assert(Geo<true>::kSmemBytes <= 232448 && Geo<false>::kSmemBytes <= 232448, "shared memory");
@@ -655,8 +657,8 @@ __device__ __noinline__ void prefetch_update_tile(const NsLaunch& p, int tile, i
 //   Poly(t)  reads A_t from Gram(t) and overwrites B, read by Apply(t-1);
 //   Apply(t) reads B_t from Poly(t), X_t from Apply(t-1), and overwrites the
 //            other X operand, read by Gram(t-1) and Apply(t-1).
-// Each epilogue warp releases one count per finished tile (16 per CTA, so 16
-// or 32 per tile), so phase ph of step s is complete when its counter reaches
+// Each warp of the epilogue group that finished a tile releases one count (8
+// per CTA, so 8 or 16 per tile), so phase ph of step s is complete when its counter reaches
 // (its tiles x releases per tile) times
 // the number of its steps up to s that this launch runs.  The counters are
 // per matrix (mode 1), or one set over all matrices (mode 2: each level then
@@ -1065,7 +1067,10 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             }
         }
     } else {
-        const int quarter = warp & 3, slice = warp >> 2;
+        // group g = warp / 8 takes the tiles of accumulator g (every other
+        // tile of the CTA's list), so one group's stores drain while the
+        // other works through the next tile
+        const int quarter = warp & 3, slice = (warp >> 2) & 1, group = warp >> 3;
         const uint32_t tempty_leader[2] = {kPair ? mapa_shared(smem_u32(&ctl->tempty[0]), 0) : 0u,
                                            kPair ? mapa_shared(smem_u32(&ctl->tempty[1]), 0) : 0u};
         bool ok = true;
@@ -1077,12 +1082,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
             const int2 range = unit_tiles(p, ph, unit);
             const bool prefetch_w = ph == kApply && step + 1 == p.steps && p.apply_update;
             for (int t = 0; t < range.y; ++t, ++q) {
+                if ((q & 1) != group) continue;           // the other group's tile
                 const TileDesc td = p.tc_tiles[ph][range.x + t];
                 const MatDesc& md = p.mats[td.mat];
-                const int acc = q & 1;
+                const int acc = group;
                 const uint32_t acc_phase = (q >> 1) & 1;
-                if (prefetch_w && t + 1 < range.y)
-                    prefetch_update_tile(p, range.x + t + 1, G::kTileRows,
+                if (prefetch_w && t + 2 < range.y)        // this group's next tile
+                    prefetch_update_tile(p, range.x + t + 2, G::kTileRows,
                                          static_cast<int>(rank) * kTcBM + quarter * 32 + lane, slice * kEpiSliceCols,
                                          lane);
                 ok = mbar_wait_bounded(smem_u32(&ctl->tfull[acc]), acc_phase, abort_flag, p.err, 0x104);
