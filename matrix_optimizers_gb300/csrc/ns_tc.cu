@@ -88,7 +88,7 @@ struct Ctl {                   // 1 KB after the ring; the store staging follows
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
-    uint64_t wbar[kEpiWarps];  // per epilogue warp: its W box has landed in its staging block
+    uint64_t wbar[kEpiWarps];  // per epilogue warp: a TMA load into its staging block has landed
     uint32_t tmem_base;
     int abort_flag;
     int dep_ready;             // tiles of this CTA's list whose inputs the dependency warp has acquired
@@ -479,11 +479,11 @@ __device__ __forceinline__ void load_diag_fix(const MatDesc& md, int step, int i
 // block through its staging block: a TMA load of W's box (32 rows x 64 B:
 // 16 fp32 or 32 bf16 columns, so an fp32 block takes two), the update in
 // shared memory, a TMA store back.  Each lane's own 32-byte row pieces of W,
-// 32 rows per warp instruction, measured about three times slower.  In the
-// transposed frame the box's rows are W's rows j0 .. j0 + 31 and a lane
-// reads a column of it.  `wuse` counts the warp's W boxes (the parity of its
-// barrier); `wpend` is set while a box may still be landing (a wait that
-// gave up), for the drain before the CTA exits.  Called by all 32 lanes.
+// 32 rows per warp instruction, took about twice as long.  In the transposed
+// frame the box's rows are W's rows j0 .. j0 + 31 and a lane reads a column
+// of it.  `wuse` counts the warp's loads into its staging block (the parity
+// of its barrier); `wpend` is set while one may still be landing (a wait
+// that gave up), for the drain before the CTA exits.  Called by all 32 lanes.
 __device__ __forceinline__ bool epi_update_tma(const NsLaunch& p, const MatDesc& md, int i0, int j0,
                                                const float (&x)[32], uint32_t sbuf, uint32_t wbar, uint32_t& wuse,
                                                bool& wpend, volatile int* abort_flag) {
@@ -1075,8 +1075,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                                            kPair ? mapa_shared(smem_u32(&ctl->tempty[1]), 0) : 0u};
         bool ok = true;
         int q = 0;
-        uint32_t wuse = 0;                        // W boxes this warp has loaded (its barrier's parity)
-        bool wpend = false;                       // a W box may still be landing after a wait gave up
+        uint32_t wuse = 0;                        // TMA loads into this warp's staging block (its barrier's parity)
+        bool wpend = false;                       // a load may still be landing after a wait gave up
         for (int lv = p.lv_begin; lv < p.lv_end && ok; ++lv) {
             const int ph = lv % 3, step = lv / 3;
             const int2 range = unit_tiles(p, ph, unit);
@@ -1150,7 +1150,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
         }
         if (lane == 0) {
             bulk_wait_all();                      // no store still reads this CTA's shared memory
-            if (wpend) {                          // nor does a W box land in it after the CTA left
+            if (wpend) {                          // nor does a load land in it after the CTA left
                 const long long t0 = clock64();
                 while (!mbar_try_wait(smem_u32(&ctl->wbar[warp]), wuse & 1u) && clock64() - t0 < kWaitCycles) {}
             }
