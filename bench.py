@@ -506,6 +506,7 @@ def run_gb300(args, rank, world, local_rank, dist):
         result["legs"] = run_legs(dev, peaks)
         result["vote_gbs"] = result["legs"]["vote"]["gbs"]
         result["vote_frac_of_hbm"] = result["legs"]["vote"]["frac"]
+        result["next_rows"] = run_next_rows(dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(shapes_all, idx)
     return result
@@ -620,6 +621,110 @@ def run_legs(dev, peaks, reps=20):
                          "l2": "inputs (1.4 GB) larger than L2"}
     out["peak_hbm_gbs"] = hbm
     out["peak_source"] = peaks["source"]
+    return out
+
+
+def run_next_rows(dev, peaks, reps=20):
+    """The rows built after the core path, timed on the device at the
+    Sign-Muon and GPT-small sizes: the local polar step on the voted signs,
+    the int8 sum vote (signs and update), and the spectral-scale variant of
+    the GPT-small step against its Frobenius form.  (The fused sign pack is
+    part of every Sign-Muon step above.)"""
+    import torch
+    import matrix_optimizers_gb300 as mo
+    from workloads import gpt_small_shapes, matrix_set_inputs, sign_muon_inputs
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    sustained = peaks["bf16_tflops_sustained"]
+
+    def per_call_ms(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for _ in range(reps):
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return float(np.median(times))
+
+    n, workers = 2048, 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    U = [torch.randn(n, n, device=dev, generator=g).bfloat16() for _ in range(workers)]
+    words = [torch.empty((n * n + 31) // 32, dtype=torch.int32, device=dev) for _ in range(workers)]
+    mo.sign_pack_batched(U, words)
+    W = torch.from_numpy(sign_muon_inputs(workers=1)["W"]).to(dev)
+
+    # local polar step: vote matrix, NS on it (5 steps), W update
+    ws = torch.empty(mo.sign_vote_polar_workspace_bytes(W), dtype=torch.uint8, device=dev)
+    t = per_call_ms(lambda: mo.sign_vote_polar_update(words, W, 1e-3, ws))
+    flops = 5 * (4 * n * n * n + 2 * n ** 3)
+    out["polar_step"] = {"what": "sign_vote_polar_update: vote of %d workers' packed signs, 5 NS steps on the "
+                                 "+-1 matrix, W update; %dx%d fp32 W" % (workers, n, n),
+                         "ms": t, "ns_tflops_nominal": flops / (t * 1e-3) / 1e12,
+                         "frac_of_sustained_nominal": flops / (t * 1e-3) / 1e12 / sustained}
+
+    # int8 sum vote: int8 signs of each worker, then the vote update, over
+    # buffer sets larger than L2 (graph of back-to-back launches)
+    sets = 3
+    S = [[torch.empty(n * n, dtype=torch.int8, device=dev) for _ in range(workers)] for _ in range(sets)]
+    Ws = [W.clone() for _ in range(sets)]
+
+    def graph_ms(fns):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for fn in fns:
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for fn in fns:
+                fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        for r in range(reps + 3):
+            e0.record()
+            gr.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            if r >= 3:
+                times.append(e0.elapsed_time(e1) / len(fns))
+        return float(np.median(times))
+
+    t_sign = graph_ms([(lambda k=k, m=m: mo.sign_int8(U[m], S[k][m])) for k in range(sets) for m in range(workers)])
+    t_vote = graph_ms([(lambda k=k: mo.sign_vote_update_int8(S[k], Ws[k], 1e-3)) for k in range(sets)])
+    b_sign = n * n * (2 + 1)
+    b_vote = workers * n * n + n * n * 8
+    out["int8_vote"] = {"what": "sign_int8 per worker (bf16 in, int8 out) and sign_vote_update_int8 over %d "
+                                "workers; %d buffer sets per graph" % (workers, sets),
+                        "sign_ms_per_worker": t_sign, "sign_frac_of_hbm": b_sign / (t_sign * 1e-3) / 1e9 / hbm,
+                        "vote_ms": t_vote, "vote_frac_of_hbm": b_vote / (t_vote * 1e-3) / 1e9 / hbm,
+                        "vote_bytes": b_vote}
+    del S, Ws, U, words, ws
+
+    # spectral-scale normalisation on the GPT-small step
+    shapes = gpt_small_shapes()
+    inputs = matrix_set_inputs(shapes)
+    Wg = [torch.from_numpy(x["W"]).to(dev) for x in inputs]
+    Mg = [torch.zeros_like(w) for w in Wg]
+    Gg = [torch.from_numpy(x["G"]).to(dev) for x in inputs]
+    mats = [mo.make_matrix(w, m, gg) for w, m, gg in zip(Wg, Mg, Gg)]
+    res = {}
+    for iters in (0, 8):
+        cfg = mo.make_cfg(mu=0.95, lr=0.02, spectral_iters=iters)
+        wsg = torch.empty(mo.mo_workspace_bytes(mats, cfg), dtype=torch.uint8, device=dev)
+        res[iters] = per_call_ms(lambda: mo.muon_step_batched(mats, cfg, wsg))
+        del wsg
+    out["spectral_scale"] = {"what": "GPT-small Muon step (72 matrices), spectral estimate with 8 power "
+                                     "iterations against Frobenius scaling",
+                             "ms_frobenius": res[0], "ms_spectral": res[8],
+                             "spectral_overhead": res[8] / res[0] - 1.0}
     return out
 
 
