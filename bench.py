@@ -93,12 +93,13 @@ def ns_flops(shape, steps=5):
 
 def ns_flops_issued(shape, steps=5):
     """MMA work actually issued: Gram and square on upper-triangular 128x256
-    tiles only (mirror-stored), apply on every tile."""
+    tiles only (mirror-stored; a tile whose first 128 columns lie below the
+    diagonal computes its last 128 only), apply on every tile."""
     m, n = min(shape), max(shape)
     tr, tc = -(-m // 128), -(-m // 256)
-    sym = sum(1 for i in range(tr) for j in range(tc) if min(j * 256 + 255, m - 1) >= i * 128)
-    tile = 128 * 256
-    return steps * (2 * sym * tile * n + 2 * sym * tile * m + 2 * m * n * m)
+    sym = sum((128 if j * 256 + 128 <= i * 128 else 256) * 128
+              for i in range(tr) for j in range(tc) if min(j * 256 + 255, m - 1) >= i * 128)
+    return steps * (2 * sym * n + 2 * sym * m + 2 * m * n * m)
 
 
 # ----------------------------------------------------------------- workloads

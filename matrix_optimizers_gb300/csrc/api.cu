@@ -303,6 +303,10 @@ Layout make_layout(const std::vector<std::pair<int64_t, int64_t>>& dims, int pre
 
 // LPT assignment of tiles to CTAs: tiles sorted by cost (descending, then
 // matrix / row / column), each to the least-loaded CTA (ties: lower index).
+// The symmetric phases' tiles whose first 128 columns lie below the diagonal
+// issue half their MMAs but keep a full epilogue; costed at half their K
+// blocks they took more tiles per CTA and measured slower (GPT-small +10%),
+// so every tile is costed by its K blocks.
 void schedule(std::vector<TileDesc>& tiles, int ctas, int epi_cost, std::vector<TileDesc>& out,
               std::vector<int2>& ranges) {
     std::stable_sort(tiles.begin(), tiles.end(), [](const TileDesc& a, const TileDesc& b) {

@@ -713,6 +713,16 @@ __device__ __noinline__ int wait_deps(const NsLaunch& p, const Deps& d, int ph, 
     }
 }
 
+// A symmetric-phase tile whose first 128 columns lie wholly below the
+// diagonal (row block 2J + 1 of column block J) computes only its last 128
+// columns: an N = 128 MMA over half of B, into the accumulator's upper 128
+// columns.  Its epilogue skips the first 128 columns as it does any block
+// below the diagonal.  Single-CTA tiles only.
+template <bool kPair>
+__device__ __forceinline__ bool half_tile(int ph, const TileDesc& td) {
+    return !kPair && ph != kApply && td.tj * kTcBN + kTcBN / 2 <= td.ti * kTcBM;
+}
+
 // Gram tiles with at least this many K blocks alternate their K direction.
 constexpr int kReverseMinKBlocks = 64;
 
@@ -885,6 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                     const bool rev = ph == kGram && td.nkb >= kReverseMinKBlocks && (t & 1);
                     const int k_last = rev ? td.nkb - 1 : 0;
                     const int k_inc = rev ? -1 : 1;
+                    const bool half = half_tile<kPair>(ph, td);
+                    const uint32_t tx = half ? static_cast<uint32_t>(2 * kABytes) : static_cast<uint32_t>(G::kTxBytes);
                     auto k_loop = [&](auto&& load) {
                         for (int kb = 0, kk = k_last; kb < td.nkb; ++kb, kk += k_inc) {
                             const uint32_t empty = smem_u32(&ctl->empty[stage]);
@@ -893,7 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                                 ok = false;
                                 return;
                             }
-                            if (leader) mbar_arrive_expect_tx(full, G::kTxBytes);
+                            if (leader) mbar_arrive_expect_tx(full, tx);
                             ++narmed;
                             const uint32_t sa = smem_u32(smem + stage * G::kStageBytes);
                             const uint32_t bar = kPair ? mapa_shared(full, 0) : full;   // the leader's barrier
@@ -901,10 +913,21 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                             if (++stage == G::kStages) { stage = 0; phase ^= 1u; }
                         }
                     };
-                    if (ph == kGram) {
+                    if (ph == kGram && half) {
+                        // B: the tile's last 128 rows, through the 128-row view
+                        k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
+                            load3<kPair>(sa, tma, bar, i0 >> 3, k0 >> 3);
+                            load3<kPair>(sb, tma, bar, (j0 + kTcBN / 2) >> 3, k0 >> 3);
+                        });
+                    } else if (ph == kGram) {
                         k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
                             load3<kPair>(sa, tma, bar, i0 >> 3, k0 >> 3);
                             load3<kPair>(sb, tmb, bar, j0 >> 3, k0 >> 3);
+                        });
+                    } else if (ph == kPoly && half) {
+                        k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
+                            load2<kPair>(sa, tma, bar, k0, i0);
+                            load2<kPair>(sb, tma, bar, k0, j0 + kTcBN / 2);
                         });
                     } else if (ph == kPoly) {
                         k_loop([&](uint32_t sa, uint32_t sb, uint32_t bar, int k0) {
@@ -985,7 +1008,13 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d = tmem + static_cast<uint32_t>(acc * kTcBN);
+                    // a half tile: N = 128 into the accumulator's last 128 columns; the
+                    // Gram phase's 128-row B block has half the column-block stride
+                    const bool half = half_tile<kPair>(ph, td);
+                    const uint32_t idesc_t = half ? idesc_bf16_f32(kTcBM, kTcBN / 2, 0u) : idesc;
+                    const uint64_t bdesc_t = half && ph == kGram ? sdesc_noswz(0, (kBRows / 2) * 16, 128) : bdesc0;
+                    const uint32_t b_step_t = half && ph == kGram ? (2 * (kBRows / 2) * 16) >> 4 : b_step;
+                    const uint32_t d = tmem + static_cast<uint32_t>(acc * kTcBN + (half ? kTcBN / 2 : 0));
                     for (int kb = 0; kb < td.nkb; ++kb) {
                         if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_flag, p.err, 0x103)) {
                             ok = false;
@@ -998,11 +1027,11 @@ __global__ void __launch_bounds__(kThreads, 1) ns_tc_kernel(const __grid_constan
                         for (int k = 0; k < kTcBK / 16; ++k) {
                             // shared addresses stay below 256 KB: the 14-bit field never carries
                             const uint64_t ad = adesc0 + ((sa >> 4) + k * a_step);
-                            const uint64_t bd = bdesc0 + ((sb >> 4) + k * b_step);
+                            const uint64_t bd = bdesc_t + ((sb >> 4) + k * b_step_t);
                             if constexpr (kPair)
-                                umma_bf16_pair(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                                umma_bf16_pair(d, ad, bd, idesc_t, (kb | k) != 0 ? 1u : 0u);
                             else
-                                umma_bf16(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                                umma_bf16(d, ad, bd, idesc_t, (kb | k) != 0 ? 1u : 0u);
                         }
                         if constexpr (kPair)
                             umma_commit_pair(smem_u32(&ctl->empty[stage]), 0x3);
