@@ -34,10 +34,12 @@ def _ns(X_list, steps=5, precision=mo.MO_NS_BF16, out_dtype=torch.float32, coeff
     return [to_np(o) for o in outs], ws, Xt
 
 
-@pytest.mark.parametrize("shape", [(256, 512), (128, 256), (200, 300), (300, 200), (64, 64)])
+@pytest.mark.parametrize("shape", [(256, 512), (128, 256), (200, 300), (300, 200), (64, 64), (640, 700)])
 def test_phases_individually(shape):
     """steps = 1: the Gram, polynomial and apply buffers each match the oracle
-    computed from the bf16 operands the kernels used."""
+    computed from the bf16 operands the kernels used.  m = 200, 256 and 640
+    include tiles whose first 128 columns lie below the diagonal (computed
+    as half tiles), 640 two of them per phase."""
     X = np.random.default_rng(1).standard_normal(shape)
     outs, ws, _ = _ns([X], steps=1)
     v = B.mo_debug_ns_view([shape], 0)
@@ -53,6 +55,8 @@ def test_phases_individually(shape):
     gram = to_np(ws_view(ws, v.gram, (m, m), torch.bfloat16, v.lda))
     want_gram = Xb @ Xb.T / s ** 2
     assert rel_fro(gram, want_gram) < 4e-3                                # bf16 storage of A
+    for r0 in range(0, m, 128):                                           # every 128-row block, on its own
+        assert rel_fro(gram[r0:r0 + 128], want_gram[r0:r0 + 128]) < 4e-3
     assert np.array_equal(gram, gram.T)                                   # mirrored exactly
     poly = to_np(ws_view(ws, v.poly, (m, m), torch.bfloat16, v.lda))
     want_poly = A * np.eye(m) + Bc * gram + C * gram @ gram              # a folded onto the diagonal
