@@ -36,8 +36,8 @@ extern "C" {
  * and polynomial, tiles_apply for apply) x (the steps of that phase the fused
  * launch ran); all three stay 0 after a call with one launch per phase.  The
  * tile counts and releases_per_tile are those of the tile geometry the
- * library uses on the current device (128 x 256 tiles per CTA, 16 releases;
- * or 256 x 256 tiles per CTA pair, 32 releases). */
+ * library uses on the current device (128 x 256 tiles per CTA, 8 releases;
+ * or 256 x 256 tiles per CTA pair, 16 releases). */
 typedef struct {
     int64_t m, n, ldx, lda;
     int32_t transposed, precision;
@@ -58,7 +58,9 @@ int mo_debug_sm_count(void);
  * on = 1 runs 256 x 256 tiles on CTA pairs (clusters of 2, tcgen05
  * cta_group::2: each CTA loads 128 rows of A and 128 columns of B) when the
  * device can co-schedule such clusters; on = 0 (the default) runs 128 x 256
- * tiles on single CTAs.  Results are identical.  Returns the previous setting, or
+ * tiles on single CTAs.  The two geometries walk K in different orders on
+ * some tiles, so they agree to fp32 accumulation noise, not bit for bit.
+ * Returns the previous setting, or
  * MO_ERR_INVALID_ARG for a value other than 0 / 1.  Process-wide. */
 int mo_debug_set_ns_pair(int on);
 
@@ -113,8 +115,8 @@ int mo_debug_cta_stamps(uint64_t* buf, int capacity, int max_ctas, int* recorded
 #define MO_K_MOMENTUM 1   /* fused momentum + norm partials (+ NS operand) */
 #define MO_K_FINALIZE 2   /* per-matrix norm finalisation */
 #define MO_K_GRAM     3   /* NS A = X X^T   (tensor cores, or CUDA cores in fp32 mode) */
-#define MO_K_POLY     4   /* NS B = bA + cA^2 */
-#define MO_K_APPLY    5   /* NS X = aX + BX (+ fused update on the last step) */
+#define MO_K_POLY     4   /* NS B = aI + bA + cA^2 (a on the diagonal) */
+#define MO_K_APPLY    5   /* NS X = BX (+ fused update on the last step) */
 #define MO_K_NS0      6   /* zero-step normalise/update */
 #define MO_K_ADAMW    7
 #define MO_K_PACK     8
