@@ -431,8 +431,14 @@ def run_gb300(args, rank, world, local_rank, dist):
         sizes = [r * c for r, c in shapes]
         # group k's share of the bytes: even, or ramped (1, 2, 4, ... up to the
         # middle and back down) so that the copy-in before the first kernel and
-        # the copy-out after the last one are short
-        if args.e2e_shape == "ramp":
+        # the copy-out after the last one are short.  auto ramps when the
+        # device step outlasts the host copies (at the 341 GB/s that pinned
+        # copies both ways at once reach on the GB300 host link): the kernels
+        # then hide the copies, and only the first and last ones show
+        shape = args.e2e_shape
+        if shape == "auto":
+            shape = "ramp" if ms_step > (h2d + d2h) / 341e9 * 1e3 else "even"
+        if shape == "ramp":
             half = [2.0 ** min(k, n_groups - 1 - k) for k in range(n_groups)]
         else:
             half = [1.0] * n_groups
@@ -497,9 +503,11 @@ def run_gb300(args, rank, world, local_rank, dist):
         ms_e2e = _max_over_ranks(e0.elapsed_time(e1) / k2, dist)
         result["e2e"] = {"value": total_mats / (ms_e2e * 1e-3), "unit": "matrices/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
-                         "steps": k2, "groups": len(groups),
-                         "path": ("pinned host G in, W out; %d size-balanced groups, one library call each, "
-                                  "copies on two side streams overlapping the kernels" % len(groups))}
+                         "steps": k2, "groups": len(groups), "group_shape": shape,
+                         "path": ("pinned host G in, W out; %d %s groups, one library call each, "
+                                  "copies on two side streams overlapping the kernels"
+                                  % (len(groups), "size-balanced" if shape == "even"
+                                     else "ramped (small first and last)"))}
         del g_ws
         del hG, hW
 
@@ -835,8 +843,9 @@ def main():
     ap.add_argument("--e2e-groups", type=int, default=0,
                     help="matrix groups of the end-to-end step (copies of one overlap the kernels of another); "
                          "0: one per ~170 MB of host traffic, 2 to 8")
-    ap.add_argument("--e2e-shape", default="even", choices=["even", "ramp"],
-                    help="byte shares of the end-to-end groups: equal, or small first and last groups")
+    ap.add_argument("--e2e-shape", default="auto", choices=["auto", "even", "ramp"],
+                    help="byte shares of the end-to-end groups: equal, small first and last groups, "
+                         "or (auto) small ones when the kernels outlast the host copies")
     ap.add_argument("--no-legs", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
