@@ -228,18 +228,33 @@ cudaError_t launch_momentum_norm(const MomLaunch& p, int grid, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------ norm_finalize
-// One warp per matrix sums its tile partials in a fixed order (float64).
-__global__ void __launch_bounds__(32) norm_finalize_kernel(const MatDesc* mats, const float* partials) {
+// One block of 256 threads per matrix sums its tile partials in a fixed order
+// (float64): thread k takes partials k, k + 256, ... in turn, then a fixed
+// pairwise tree combines the 256 sums.  One warp per matrix would wait on
+// 32 rounds of L2 loads for a 2048 x 2048 matrix (1024 partials) and 344 for
+// a 4096 x 11008 one.
+constexpr int kFinThreads = 256;
+__global__ void __launch_bounds__(kFinThreads) norm_finalize_kernel(const MatDesc* mats, const float* partials) {
+    __shared__ double red[kFinThreads];
     const MatDesc& md = mats[blockIdx.x];
+    const int k = threadIdx.x;
     const int64_t nt = static_cast<int64_t>(md.mom_tiles_r) * md.mom_tiles_c;
+    const float* part = partials + md.mom_tile_begin;
     double s = 0.0;
-    for (int64_t i = threadIdx.x; i < nt; i += 32) s += static_cast<double>(partials[md.mom_tile_begin + i]);
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (threadIdx.x == 0) {
+#pragma unroll 4
+    for (int64_t i = k; i < nt; i += kFinThreads) s += static_cast<double>(part[i]);
+    red[k] = s;
+    __syncthreads();
+    for (int w = kFinThreads / 2; w > 0; w >>= 1) {
+        if (k < w) red[k] += red[k + w];
+        __syncthreads();
+    }
+    if (k == 0) {
+        const double t = red[0];
         float inv_s = 0.f, inv_s2 = 0.f;
-        if (s > 0.0) {
-            inv_s = static_cast<float>(1.0 / sqrt(s));
-            inv_s2 = static_cast<float>(1.0 / s);
+        if (t > 0.0) {
+            inv_s = static_cast<float>(1.0 / sqrt(t));
+            inv_s2 = static_cast<float>(1.0 / t);
         }
         md.scales[0] = inv_s;
         md.scales[1] = inv_s2;
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(32) norm_finalize_kernel(const MatDesc* mats, 
 
 cudaError_t launch_norm_finalize(const MatDesc* mats, int nmats, const float* partials, cudaStream_t s) {
     if (nmats == 0) return cudaSuccess;
-    norm_finalize_kernel<<<nmats, 32, 0, s>>>(mats, partials);
+    norm_finalize_kernel<<<nmats, kFinThreads, 0, s>>>(mats, partials);
     return cudaGetLastError();
 }
 
