@@ -186,10 +186,10 @@ int ns_orthogonalize(const void* const* X, void* const* out,
  *   - Every call shares the one array per device and it keeps the last
  *     call's contents; calls whose work overlaps on the GPU (other streams,
  *     other threads) race and corrupt each other's results.
- *   - No cudaMalloc, cudaFree or other allocating routine is called.  The
- *     device error word is not exposed for this entry point: a run whose
- *     bounded device waits expire (about 2 s) leaves `out` unspecified and
- *     still returns MO_OK.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ *   - A run whose bounded device waits expire (about 2 s) leaves `out`
+ *     unspecified and still returns MO_OK (the wait happens on the GPU after
+ *     the call returned); ns_orthogonalize_noalloc_status reports it.
  *   - The call's small control block is copied from ordinary (pageable)
  *     host memory with cudaMemcpyAsync, so the call may return only once
  *     that copy has been staged: it is not fully asynchronous to the host.
@@ -200,6 +200,13 @@ int ns_orthogonalize(const void* const* X, void* const* out,
 int ns_orthogonalize_noalloc(const void* X, void* out, int64_t rows, int64_t cols, int64_t ld,
                              int in_dtype, int out_dtype, int steps, float a, float b, float c,
                              mo_stream_t stream);
+
+/* Status of the allocation-free runs on the current device: waits for
+ * `stream`, then returns MO_ERR_TIMEOUT if a run's bounded device wait gave
+ * up since the last check (and clears that record), else MO_OK; MO_ERR_CUDA
+ * if the device cannot be queried.  As mo_check_device_status, applied to the
+ * fixed scratch; it allocates nothing. */
+int ns_orthogonalize_noalloc_status(mo_stream_t stream);
 
 /* Sign extraction and 1-bit packing (SignMuon §2 step 2 and the all-gather
  * variant of step 3).  Element j of the row-major flattening of U (rows x

@@ -79,6 +79,7 @@ _SIGNATURES = [
                                    c_float, c_float, c_float, c_int32, c_void_p, c_size_t, c_void_p]),
     ("ns_orthogonalize_noalloc", c_int32, [c_void_p, c_void_p, c_int64, c_int64, c_int64, c_int32, c_int32,
                                            c_int32, c_float, c_float, c_float, c_void_p]),
+    ("ns_orthogonalize_noalloc_status", c_int32, [c_void_p]),
     ("sign_pack", c_int32, [c_void_p, c_int32, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     ("sign_vote_update", c_int32, [ctypes.POINTER(c_void_p), c_int32, c_int64, c_int64, c_void_p,
                                    c_int32, c_int64, c_float, c_void_p]),
@@ -279,6 +280,12 @@ def ns_orthogonalize_noalloc(X, out, steps, a=3.4445, b=-4.7750, c=2.0315, strea
     _check(load().ns_orthogonalize_noalloc(_ptr(X), _ptr(out), X.size(0), X.size(1), _ld(X),
                                            dtype_code(X.dtype), dtype_code(out.dtype), steps, a, b, c,
                                            _stream(stream)))
+
+
+def ns_orthogonalize_noalloc_status(stream=None):
+    """MO_OK, or MO_ERR_TIMEOUT if an allocation-free run's bounded device
+    wait gave up since the last check (the record is then cleared)."""
+    return load().ns_orthogonalize_noalloc_status(_stream(stream))
 
 
 def sign_pack(U, words, stream=None):

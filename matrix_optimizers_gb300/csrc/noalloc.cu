@@ -53,3 +53,10 @@ extern "C" int ns_orthogonalize_noalloc(const void* X, void* out, int64_t rows, 
     return ns_orthogonalize(&X, &out, &rows, &cols, &ld, 1, in_dtype, out_dtype, steps, a, b, c, MO_NS_BF16, ws,
                             MO_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+extern "C" int ns_orthogonalize_noalloc_status(mo_stream_t stream) {
+    void* ws = nullptr;
+    const int st = scratch_address(&ws);
+    if (st != MO_OK) return st;
+    return mo_check_device_status(ws, stream);
+}

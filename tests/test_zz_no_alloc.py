@@ -48,6 +48,8 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
         # the second call takes no device memory at all (the first may have
         # loaded the library's module and its scratch array)
         assert torch.cuda.mem_get_info()[0] == free_after_first
+        # the runs' device status: no bounded wait gave up
+        assert B.ns_orthogonalize_noalloc_status() == B.MO_OK
         for out in outs:
             got = to_np(out)
             assert np.all(np.isfinite(got))
