@@ -678,7 +678,19 @@ int run_ns(const std::vector<Job>& jobs, const NsOpts& o, void* ws, size_t ws_by
     mp.fp32_operand = o.precision == MO_NS_FP32;
     mp.partials = reinterpret_cast<float*>(base + L.partials);
     const int mom_grid = static_cast<int>(std::min<int64_t>(L.mom_tiles, static_cast<int64_t>(nsm) * 8));
-    e = traced(MO_K_MOMENTUM, stream, [&] { return launch_momentum_norm(mp, mom_grid, stream); });
+    // bf16 momentum with an fp32 gradient, untransposed and 16-byte aligned
+    // throughout: the kernel with 16-byte momentum accesses
+    bool bf16m = o.precision == MO_NS_BF16;
+    for (const Job& j : jobs)
+        bf16m = bf16m && j.has_momentum && j.src_dtype == MO_BF16 && j.g_dtype == MO_F32 && j.rows <= j.cols &&
+                j.ld % 8 == 0 && reinterpret_cast<uintptr_t>(j.src) % 16 == 0 &&
+                reinterpret_cast<uintptr_t>(j.grad) % 16 == 0;
+    if (bf16m) {
+        const int grid6 = static_cast<int>(std::min<int64_t>(L.mom_tiles, static_cast<int64_t>(nsm) * 6));
+        e = traced(MO_K_MOMENTUM, stream, [&] { return launch_momentum_norm_bf16m(mp, grid6, stream); });
+    } else {
+        e = traced(MO_K_MOMENTUM, stream, [&] { return launch_momentum_norm(mp, mom_grid, stream); });
+    }
     if (e != cudaSuccess) return MO_ERR_CUDA;
     e = traced(MO_K_FINALIZE, stream, [&] { return launch_norm_finalize(dmats, mp.nmats, mp.partials, stream); });
     if (e != cudaSuccess) return MO_ERR_CUDA;

@@ -221,6 +221,77 @@ __global__ void __launch_bounds__(256, 8) momentum_norm_kernel(MomLaunch p) {
     }
 }
 
+// Momentum stored in bf16 with an fp32 gradient, untransposed, bf16 operand
+// (the Sign-Muon workers): 8 consecutive columns per thread, so each of its
+// accesses is one 16-byte run (the momentum, the operand's 8-column block
+// row) or two (the gradient), where the general kernel's 4 columns of bf16
+// give 8-byte momentum accesses.  The host picks this kernel only when every
+// matrix of the call qualifies: bf16 momentum, fp32 gradient, rows <= cols,
+// ld a multiple of 8 and 16-byte aligned momentum and gradient.
+// Tile of 64 x 64 as above; thread t owns columns 8*(t%8)..+7 of rows
+// t/8 + 32q, q = 0, 1.  The tile's sum of squares runs in this fixed order.
+__global__ void __launch_bounds__(256, 6) momentum_norm_bf16m_kernel(MomLaunch p) {
+    __shared__ float red[8];
+    const int col8 = threadIdx.x & 7, rsub = threadIdx.x >> 3;
+    for (int64_t t = blockIdx.x; t < p.ntiles; t += gridDim.x) {
+        const MatDesc& md = p.mats[find_matrix(p.mats, p.nmats, t)];
+        const int64_t local = t - md.mom_tile_begin;
+        const int r0 = static_cast<int>(local / md.mom_tiles_c) * kMomTile;
+        const int c0 = static_cast<int>(local % md.mom_tiles_c) * kMomTile;
+        const int c = c0 + 8 * col8;
+        const int nvalid = max(0, min(8, md.cols - c));
+        float ss = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+            const int r = r0 + rsub + 32 * q;
+            if (r >= md.rows || nvalid <= 0) continue;
+            const int64_t off = static_cast<int64_t>(r) * md.ld + c;
+            float x[8];
+            if (nvalid == 8) {
+                const uint4 mv = *reinterpret_cast<const uint4*>(static_cast<const bf16*>(md.src) + off);
+                const float4 g0 = *reinterpret_cast<const float4*>(static_cast<const float*>(md.grad) + off);
+                const float4 g1 = *reinterpret_cast<const float4*>(static_cast<const float*>(md.grad) + off + 4);
+                const __nv_bfloat162* mh = reinterpret_cast<const __nv_bfloat162*>(&mv);
+                const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+                uint4 xv;
+                uint32_t* xw = reinterpret_cast<uint32_t*>(&xv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(fmaf(p.mu, __low2float(mh[q]), g[2 * q]),
+                                                                   fmaf(p.mu, __high2float(mh[q]), g[2 * q + 1]));
+                    xw[q] = *reinterpret_cast<const uint32_t*>(&h);
+                    x[2 * q] = __low2float(h);
+                    x[2 * q + 1] = __high2float(h);
+                }
+                *reinterpret_cast<uint4*>(static_cast<bf16*>(md.src) + off) = xv;
+                *reinterpret_cast<uint4*>(static_cast<bf16*>(md.x_op[0]) + xop_offset(md, false, r, c)) = xv;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    x[k] = 0.f;
+                    if (k < nvalid) {
+                        const float m = load_elem(md.src, MO_BF16, off + k);
+                        const float g = load_elem(md.grad, MO_F32, off + k);
+                        x[k] = __bfloat162float(__float2bfloat16_rn(fmaf(p.mu, m, g)));
+                        store_elem(md.src, MO_BF16, off + k, x[k]);
+                        store_elem(md.x_op[0], MO_BF16, xop_offset(md, false, r, c + k), x[k]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) ss = fmaf(x[k], x[k], ss);
+        }
+        const float total = block_sum_256(ss, red);
+        if (threadIdx.x == 0) p.partials[t] = total;
+    }
+}
+
+cudaError_t launch_momentum_norm_bf16m(const MomLaunch& p, int grid, cudaStream_t s) {
+    if (p.ntiles == 0) return cudaSuccess;
+    momentum_norm_bf16m_kernel<<<grid, 256, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_momentum_norm(const MomLaunch& p, int grid, cudaStream_t s) {
     if (p.ntiles == 0) return cudaSuccess;
     momentum_norm_kernel<<<grid, 256, 0, s>>>(p);

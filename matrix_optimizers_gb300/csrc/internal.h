@@ -137,6 +137,8 @@ struct MomLaunch {
 
 // ------------------------------------------------------------------ launchers
 cudaError_t launch_momentum_norm(const MomLaunch& p, int grid, cudaStream_t s);
+// bf16 momentum, fp32 gradient, rows <= cols, ld % 8 == 0, 16-byte aligned M and G (6 blocks per SM)
+cudaError_t launch_momentum_norm_bf16m(const MomLaunch& p, int grid, cudaStream_t s);
 cudaError_t launch_norm_finalize(const MatDesc* mats, int nmats, const float* partials,
                                  cudaStream_t s);
 cudaError_t launch_ns_k0(const MomLaunch& p, float alpha, float decay, int apply_update, int grid,

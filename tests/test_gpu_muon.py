@@ -6,6 +6,7 @@ import torch
 
 import matrix_optimizers_gb300 as mo
 from oracle import adamw as oa
+from oracle.bf16 import round_bf16
 from oracle import muon as om
 from oracle import planner as oplan
 from oracle import sign as osg
@@ -123,6 +124,55 @@ def test_bf16_state_dtypes():
     # W is stored in bf16: compare the update with bf16 storage noise allowed
     assert rel_fro(to_np(W) - W0, Wn - W0) < 3e-2
     assert rel_fro(to_np(M), Mn) < 4e-3
+
+
+def _bf16_ulp(x):
+    """Spacing of bfloat16 at |x| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(x), np.finfo(np.float32).tiny)))
+    return np.exp2(e - 7)
+
+
+@pytest.mark.parametrize("shapes", [
+    # every matrix untransposed with ld % 8 == 0: the 16-byte momentum kernel
+    [(192, 256, 256), (70, 203, 208), (130, 130, 136), (64, 1000, 1000)],
+    # a transposed matrix in the batch: the general kernel for all of them
+    [(192, 256, 256), (70, 203, 208), (300, 100, 104)],
+])
+def test_bf16_momentum_fp32_gradient(shapes):
+    """bf16 momentum with an fp32 gradient (the Sign-Muon workers' state):
+    the stored momentum is bf16(mu*M + G), the oracle's value or the bf16
+    neighbour that the fp32 fma's double rounding can give, and the update
+    matches the oracle's Muon step on that momentum.  Ragged columns (the last
+    8-column group partly valid), padded leading dimensions and tiles cut at
+    the matrix edge, and a batch that the 16-byte kernel does not take."""
+    rng = np.random.default_rng(sum(r * c for r, c, _ in shapes))
+    mats, keep = [], []
+    for rows, cols, ld in shapes:
+        W0 = (0.02 * rng.standard_normal((rows, cols))).astype(np.float32)
+        M0 = round_bf16(rng.standard_normal((rows, cols))).astype(np.float32)
+        G0 = rng.standard_normal((rows, cols)).astype(np.float32)
+
+        def padded(a, dtype):
+            big = torch.zeros((rows, ld), dtype=dtype, device=dev())
+            big[:, :cols] = to_dev(a, dtype)
+            return big[:, :cols]
+
+        W, M, G = padded(W0, torch.float32), padded(M0, torch.bfloat16), padded(G0, torch.float32)
+        assert np.array_equal(to_np(M), M0)
+        mats.append(mo.make_matrix(W, M, G))
+        keep.append((W, M, G, W0, M0, G0))
+    cfg = mo.make_cfg(mu=0.95, lr=0.05)
+    ws = workspace(mo.mo_workspace_bytes(mats, cfg))
+    mo.muon_step_batched(mats, cfg, ws)
+    torch.cuda.synchronize()
+    assert mo.mo_check_device_status(ws) == 0
+    for (rows, cols, _), (W, M, G, W0, M0, G0) in zip(shapes, keep):
+        Wn, Mn, _ = om.muon_step(W0.astype(np.float64), M0.astype(np.float64), G0.astype(np.float64),
+                                 mu=0.95, lr=0.05, m_dtype="bf16")
+        got = to_np(M).astype(np.float64)
+        assert np.all(np.abs(got - Mn) <= _bf16_ulp(Mn)), (rows, cols)
+        assert np.mean(got == Mn) > 0.99, (rows, cols)
+        assert rel_fro(to_np(W) - W0, Wn - W0) < NS_BF16_TOL, (rows, cols)
 
 
 @pytest.mark.parametrize("rows,cols,ld,wdt", [
